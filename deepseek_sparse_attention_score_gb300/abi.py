@@ -1,0 +1,295 @@
+"""Thin Python binding of the C ABI in ``include/dsa.h``.
+
+Every function here has the name of the C entry point it wraps and does
+argument marshalling only: shape/dtype/device checks, optional allocation of
+output and workspace tensors with PyTorch, the ctypes call on the current CUDA
+stream, and turning a negative return code into an exception. All arithmetic
+runs in the CUDA kernels of ``libdsa_gb300.so``; there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdsa_gb300.so")
+
+ERRORS = {
+    -1: "DSA_ERR_INVALID_ARGUMENT",
+    -2: "DSA_ERR_UNSUPPORTED",
+    -3: "DSA_ERR_WORKSPACE",
+    -4: "DSA_ERR_CUDA",
+    -5: "DSA_ERR_SHARED_BEFORE_FULL",
+    -6: "DSA_ERR_BAD_INDEXER_TYPE",
+    -7: "DSA_ERR_ALIGNMENT",
+}
+STATUS_UNION_TRUNCATED = 0x1
+STATUS_BAD_METADATA = 0x2
+STATUS_BAD_INDEX = 0x4
+STATUS_TIMEOUT = 0x8
+STATUS_INTERNAL = 0x10
+
+EXPORTS = (
+    "dsa_index_build_share_map",
+    "dsa_indexer_workspace_size",
+    "dsa_indexer_topk",
+    "dsa_indexer_page_topk",
+    "dsa_build_block_union",
+    "dsa_sparse_mla_decode_workspace_size",
+    "dsa_sparse_mla_decode",
+    "dsa_sparse_mla_prefill_qblock",
+    "dsa_device_sm_count",
+    "dsa_launch_count",
+)
+
+
+class DSAError(RuntimeError):
+    def __init__(self, fn, rc):
+        super().__init__(f"{fn} returned {rc} ({ERRORS.get(rc, 'unknown')})")
+        self.rc = rc
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_Z = ctypes.c_size_t
+_F = ctypes.c_float
+
+
+def lib() -> ctypes.CDLL:
+    """Load the in-tree library (built by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
+            "(there is no non-CUDA implementation of this package)")
+    L = ctypes.CDLL(LIB_PATH)
+    L.dsa_index_build_share_map.argtypes = [_P, _I, _I, _P, _P, _P]
+    L.dsa_indexer_workspace_size.argtypes = [_I, _I, _I, _I]
+    L.dsa_indexer_workspace_size.restype = _Z
+    L.dsa_indexer_topk.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P,
+                                   _Z, _P]
+    L.dsa_indexer_page_topk.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I,
+                                        _P, _P, _P, _Z, _P]
+    L.dsa_build_block_union.argtypes = [_P, _P, _I, _I, _I, _I, _P, _P, _I, _I, _I, _P, _P, _P, _P]
+    L.dsa_sparse_mla_decode_workspace_size.argtypes = [_I, _I, _I]
+    L.dsa_sparse_mla_decode_workspace_size.restype = _Z
+    L.dsa_sparse_mla_decode.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                                        _F, _P, _P, _P, _Z, _P]
+    L.dsa_sparse_mla_prefill_qblock.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                                _I, _I, _I, _I, _F, _P, _P, _P]
+    L.dsa_device_sm_count.argtypes = []
+    L.dsa_launch_count.argtypes = []
+    L.dsa_launch_count.restype = ctypes.c_longlong
+    for name in EXPORTS:
+        if name not in ("dsa_indexer_workspace_size", "dsa_sparse_mla_decode_workspace_size",
+                        "dsa_launch_count"):
+            getattr(L, name).restype = _I
+    _lib = L
+    return L
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(fn, rc):
+    if rc != 0:
+        raise DSAError(fn, rc)
+
+
+def _need(t, name, dtype, device, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+
+
+def _meta(device, seq_lens, cu_q_lens, cu_kv_lens, page_indices):
+    for n, t in (("seq_lens", seq_lens), ("cu_q_lens", cu_q_lens), ("cu_kv_lens", cu_kv_lens),
+                 ("page_indices", page_indices)):
+        _need(t, n, torch.int32, device, 1)
+    return seq_lens.numel(), page_indices.numel()
+
+
+# --------------------------------------------------------------------- host
+def dsa_index_build_share_map(indexer_types, num_layers, skip_offset=0):
+    """IndexShare layer -> slot map. ``indexer_types``: sequence of 0 (full) /
+    1 (shared), or None for all full. Returns (full_slot, src_slot, num_full)
+    as Python lists / int (full_slot is -1 on shared layers)."""
+    L = lib()
+    types = None
+    if indexer_types is not None:
+        types = (ctypes.c_int32 * num_layers)(*[int(x) for x in indexer_types])
+    full = (ctypes.c_int32 * max(1, num_layers))()
+    src = (ctypes.c_int32 * max(1, num_layers))()
+    nf = ctypes.c_int32(0)
+    rc = L.dsa_index_build_share_map(types, num_layers, skip_offset, full, src, ctypes.byref(nf))
+    _check("dsa_index_build_share_map", rc)
+    return list(full)[:num_layers], list(src)[:num_layers], nf.value
+
+
+def dsa_indexer_workspace_size(T, S, max_kv, ps):
+    return int(lib().dsa_indexer_workspace_size(T, S, max_kv, ps))
+
+
+def dsa_sparse_mla_decode_workspace_size(T, H, Dv=512):
+    return int(lib().dsa_sparse_mla_decode_workspace_size(T, H, Dv))
+
+
+def dsa_device_sm_count():
+    return int(lib().dsa_device_sm_count())
+
+
+def dsa_launch_count():
+    return int(lib().dsa_launch_count())
+
+
+# ------------------------------------------------------------------ indexer
+def dsa_indexer_topk(q, w, kcache, seq_lens, cu_q_lens, cu_kv_lens, page_indices, *, k, max_kv, topk=None,
+                     topk_scores=None, want_scores=False, ws=None, dev_status=None):
+    """Indexer score + exact token top-k. Returns ``topk`` (and the scores of
+    the selected positions when ``want_scores`` or ``topk_scores`` is given)."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev, 3)
+    _need(w, "w", torch.float32, dev, 2)
+    _need(kcache, "kcache", torch.bfloat16, dev, 3)
+    S, PTW = _meta(dev, seq_lens, cu_q_lens, cu_kv_lens, page_indices)
+    T, Hi, Di = q.shape
+    P, ps, _ = kcache.shape
+    if topk is None:
+        topk = torch.empty((T, k), dtype=torch.int32, device=dev)
+    if want_scores and topk_scores is None:
+        topk_scores = torch.empty((T, k), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = torch.empty(max(1, dsa_indexer_workspace_size(T, S, max_kv, ps)), dtype=torch.uint8, device=dev)
+    rc = lib().dsa_indexer_topk(_stream(dev), _ptr(q), _ptr(w), _ptr(kcache), _ptr(seq_lens), _ptr(cu_q_lens),
+                                _ptr(cu_kv_lens), _ptr(page_indices), T, S, P, PTW, ps, Hi, Di, max_kv, k,
+                                _ptr(topk), _ptr(topk_scores), _ptr(ws), ws.numel(), _ptr(dev_status))
+    _check("dsa_indexer_topk", rc)
+    return (topk, topk_scores) if topk_scores is not None else topk
+
+
+def dsa_indexer_page_topk(q, w, kcache, seq_lens, cu_q_lens, cu_kv_lens, page_indices, *, k_pages, max_kv,
+                          topk_pages=None, k=0, topk=None, with_tokens=False, topk_scores=None, ws=None,
+                          dev_status=None):
+    """Indexer score + page top-k (max-pooled per page); with ``with_tokens``
+    (or a ``topk`` tensor) also the token top-k from the same score pass.
+    Returns ``topk_pages`` or ``(topk_pages, topk)``."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev, 3)
+    _need(w, "w", torch.float32, dev, 2)
+    _need(kcache, "kcache", torch.bfloat16, dev, 3)
+    S, PTW = _meta(dev, seq_lens, cu_q_lens, cu_kv_lens, page_indices)
+    T, Hi, Di = q.shape
+    P, ps, _ = kcache.shape
+    if topk_pages is None:
+        topk_pages = torch.empty((T, k_pages), dtype=torch.int32, device=dev)
+    if with_tokens and topk is None:
+        topk = torch.empty((T, k), dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = torch.empty(max(1, dsa_indexer_workspace_size(T, S, max_kv, ps)), dtype=torch.uint8, device=dev)
+    rc = lib().dsa_indexer_page_topk(_stream(dev), _ptr(q), _ptr(w), _ptr(kcache), _ptr(seq_lens),
+                                     _ptr(cu_q_lens), _ptr(cu_kv_lens), _ptr(page_indices), T, S, P, PTW, ps, Hi,
+                                     Di, max_kv, k_pages, _ptr(topk_pages), k, _ptr(topk), _ptr(topk_scores),
+                                     _ptr(ws), ws.numel(), _ptr(dev_status))
+    _check("dsa_indexer_page_topk", rc)
+    return (topk_pages, topk) if topk is not None else topk_pages
+
+
+# -------------------------------------------------------------------- union
+def dsa_build_block_union(topk_units, *, QB, u_max=0, cu_q_lens=None, cu_kv_lens=None, ps=64, PTW,
+                          units=None, member=None, counts=None, dev_status=None):
+    """Per-block sorted union, bit-packed slot-major membership and true
+    counts. Returns (units [nQB,u_max], member [nQB,u_max,QB/32] int32 view of
+    the uint32 words, counts [nQB])."""
+    dev = topk_units.device
+    _need(topk_units, "topk_units", torch.int32, dev, 2)
+    T, K = topk_units.shape
+    S = 0
+    if cu_q_lens is not None:
+        _need(cu_q_lens, "cu_q_lens", torch.int32, dev, 1)
+        _need(cu_kv_lens, "cu_kv_lens", torch.int32, dev, 1)
+        S = cu_q_lens.numel() - 1
+    if u_max <= 0:
+        u_max = min(QB * K, PTW)
+    nqb = (T + QB - 1) // QB
+    if units is None:
+        units = torch.empty((nqb, u_max), dtype=torch.int32, device=dev)
+    if member is None:
+        member = torch.empty((nqb, u_max, QB // 32), dtype=torch.int32, device=dev)
+    if counts is None:
+        counts = torch.empty((nqb,), dtype=torch.int32, device=dev)
+    rc = lib().dsa_build_block_union(_stream(dev), _ptr(topk_units), T, K, QB, u_max, _ptr(cu_q_lens),
+                                     _ptr(cu_kv_lens), S, ps, PTW, _ptr(units), _ptr(member), _ptr(counts),
+                                     _ptr(dev_status))
+    _check("dsa_build_block_union", rc)
+    return units, member, counts
+
+
+# ------------------------------------------------------------------- attend
+def dsa_sparse_mla_decode(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, sel, *, unit, sm_scale, o=None,
+                          lse=None, want_lse=False, ws=None, dev_status=None, Dv=512):
+    """Sparse absorbed-MLA attention over per-query selections (token ids when
+    ``unit == 1``, sequence-local pages when ``unit == page_size``)."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev, 3)
+    _need(kv, "kv", torch.bfloat16, dev, 3)
+    _need(sel, "sel", torch.int32, dev, 2)
+    S, PTW = _meta(dev, seq_lens, cu_q_lens, cu_kv_lens, page_indices)
+    T, H, Dk = q.shape
+    P, ps, row_stride = kv.shape
+    K = sel.shape[1]
+    if o is None:
+        o = torch.empty((T, H, Dv), dtype=torch.bfloat16, device=dev)
+    if want_lse and lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if ws is None:
+        nb = dsa_sparse_mla_decode_workspace_size(T, H, Dv)
+        ws = torch.empty(max(1, nb), dtype=torch.uint8, device=dev)
+    rc = lib().dsa_sparse_mla_decode(_stream(dev), _ptr(q), _ptr(kv), row_stride, _ptr(seq_lens), _ptr(cu_q_lens),
+                                     _ptr(cu_kv_lens), _ptr(page_indices), _ptr(sel), K, unit, T, S, P, PTW, ps, H,
+                                     Dk, Dv, float(sm_scale), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(),
+                                     _ptr(dev_status))
+    _check("dsa_sparse_mla_decode", rc)
+    return (o, lse) if lse is not None else o
+
+
+def dsa_sparse_mla_prefill_qblock(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, units, member, counts, *,
+                                  QB, sm_scale, o=None, lse=None, want_lse=False, dev_status=None, Dv=512):
+    """Query-block sparse-MLA prefill over the union tables of
+    ``dsa_build_block_union`` (same QB and u_max)."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev, 3)
+    _need(kv, "kv", torch.bfloat16, dev, 3)
+    _need(units, "units", torch.int32, dev, 2)
+    _need(member, "member", torch.int32, dev, 3)
+    _need(counts, "counts", torch.int32, dev, 1)
+    S, PTW = _meta(dev, seq_lens, cu_q_lens, cu_kv_lens, page_indices)
+    T, H, Dk = q.shape
+    P, ps, row_stride = kv.shape
+    u_max = units.shape[1]
+    if o is None:
+        o = torch.empty((T, H, Dv), dtype=torch.bfloat16, device=dev)
+    if want_lse and lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    rc = lib().dsa_sparse_mla_prefill_qblock(_stream(dev), _ptr(q), _ptr(kv), row_stride, _ptr(seq_lens),
+                                             _ptr(cu_q_lens), _ptr(cu_kv_lens), _ptr(page_indices), _ptr(units),
+                                             _ptr(member), _ptr(counts), QB, u_max, T, S, P, PTW, ps, H, Dk, Dv,
+                                             float(sm_scale), _ptr(o), _ptr(lse), _ptr(dev_status))
+    _check("dsa_sparse_mla_prefill_qblock", rc)
+    return (o, lse) if lse is not None else o

@@ -1,0 +1,247 @@
+// extern "C" entry points of include/dsa.h: host-side argument checks,
+// workspace carving, and the kernel launches of each operation.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "attend.cuh"
+#include "common.cuh"
+#include "indexer.cuh"
+
+namespace dsa {
+
+static std::atomic<long long> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool ps_supported(int ps) { return ps == 32 || ps == 64 || ps == 128; }
+
+static int check_meta(const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
+                      const int32_t* page_indices, int T, int S, int P, int PTW, int ps) {
+  if (T < 0 || S < 0 || P < 0 || PTW < 0) return DSA_ERR_INVALID_ARGUMENT;
+  if (T > 0 && (S < 1 || P < 1 || PTW < 1)) return DSA_ERR_INVALID_ARGUMENT;
+  if (T > 0 && (!seq_lens || !cu_q_lens || !cu_kv_lens || !page_indices)) return DSA_ERR_INVALID_ARGUMENT;
+  if (!ps_supported(ps)) return DSA_ERR_UNSUPPORTED;
+  if ((long long)P * ps >= (1LL << 31)) return DSA_ERR_UNSUPPORTED;
+  return DSA_OK;
+}
+
+static int indexer_common(cudaStream_t stream, const uint16_t* q, const float* w, const uint16_t* kcache,
+                          const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
+                          const int32_t* page_indices, int T, int S, int P, int PTW, int ps, int Hi, int Di,
+                          int max_kv, int k_pages, int32_t* topk_pages, int k, int32_t* topk, float* topk_scores,
+                          void* ws, size_t ws_bytes, int32_t* dev_status) {
+  int rc = check_meta(seq_lens, cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps);
+  if (rc) return rc;
+  if (Hi != 32 || Di != 128) return DSA_ERR_UNSUPPORTED;
+  if (max_kv < 1) return DSA_ERR_INVALID_ARGUMENT;
+  if (topk && k < 1) return DSA_ERR_INVALID_ARGUMENT;
+  if (topk_pages && k_pages < 1) return DSA_ERR_INVALID_ARGUMENT;
+  if (!topk && !topk_pages) return DSA_ERR_INVALID_ARGUMENT;
+  if (T == 0) return DSA_OK;
+  if (!q || !w || !kcache) return DSA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(w) || !aligned16(kcache)) return DSA_ERR_ALIGNMENT;
+  if (T >= (1 << 24) || S >= (1 << 24)) return DSA_ERR_UNSUPPORTED;
+  const IndexerLayout L = indexer_layout(T, S, max_kv, ps);
+  if (!ws || ws_bytes < L.total || !aligned16(ws)) return DSA_ERR_WORKSPACE;
+  IndexerMeta m{w, seq_lens, cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps, max_kv, dev_status};
+  IndexerPlan pl;
+  IndexerOut out;
+  rc = run_indexer(stream, m, q, kcache, ws, L, topk != nullptr, topk_pages != nullptr, &pl, &out);
+  if (rc) return rc;
+  if (topk) {
+    rc = run_topk(stream, out.tok_scores, out.ld_tok, pl.nvis, T, 1, k, topk, topk_scores, max_kv);
+    if (rc) return rc;
+  }
+  if (topk_pages) {
+    rc = run_topk(stream, out.page_scores, out.ld_pg, pl.nvis, T, ps, k_pages, topk_pages, nullptr,
+                  (max_kv + ps - 1) / ps);
+    if (rc) return rc;
+  }
+  return DSA_OK;
+}
+
+static int attend_check(const uint16_t* q, const uint16_t* kv, int row_stride, int T, int H, int Dk, int Dv,
+                        uint16_t* o) {
+  if (H < 0) return DSA_ERR_INVALID_ARGUMENT;
+  if (Dk != 576 || Dv != 512) return DSA_ERR_UNSUPPORTED;
+  if (row_stride != 576 && row_stride != 640) return DSA_ERR_UNSUPPORTED;
+  if (T > 0 && H > 0 && (!q || !kv || !o)) return DSA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(kv) || !aligned16(o)) return DSA_ERR_ALIGNMENT;
+  if (T > 65535) return DSA_ERR_UNSUPPORTED;  // grid.y
+  return DSA_OK;
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+int dsa_device_sm_count(void) { return sm_count(); }
+long long dsa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int dsa_index_build_share_map(const int32_t* types, int num_layers, int skip_offset, int32_t* full_slot,
+                              int32_t* src_slot, int32_t* num_full) {
+  (void)skip_offset;  // accepted and unused, as in the reference map builder
+  if (num_layers < 0 || !full_slot || !src_slot || !num_full) return DSA_ERR_INVALID_ARGUMENT;
+  int last = -1, nfull = 0;
+  for (int l = 0; l < num_layers; ++l) {
+    const int ty = types ? types[l] : 0;
+    if (ty == 0) {
+      last = nfull++;
+      full_slot[l] = last;
+      src_slot[l] = last;
+    } else if (ty == 1) {
+      if (last < 0) return DSA_ERR_SHARED_BEFORE_FULL;
+      full_slot[l] = -1;
+      src_slot[l] = last;
+    } else {
+      return DSA_ERR_BAD_INDEXER_TYPE;
+    }
+  }
+  *num_full = nfull;
+  return DSA_OK;
+}
+
+size_t dsa_indexer_workspace_size(int T, int S, int max_kv, int ps) {
+  if (T < 0 || S < 0 || max_kv < 1 || !ps_supported(ps)) return 0;
+  return indexer_layout(T, S, max_kv, ps).total;
+}
+
+int dsa_indexer_topk(dsa_stream_t stream, const uint16_t* q, const float* w, const uint16_t* kcache,
+                     const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
+                     const int32_t* page_indices, int T, int S, int P, int PTW, int ps, int Hi, int Di, int max_kv,
+                     int k, int32_t* topk, float* topk_scores, void* ws, size_t ws_bytes, int32_t* dev_status) {
+  if (!topk) return DSA_ERR_INVALID_ARGUMENT;
+  return indexer_common(static_cast<cudaStream_t>(stream), q, w, kcache, seq_lens, cu_q_lens, cu_kv_lens,
+                        page_indices, T, S, P, PTW, ps, Hi, Di, max_kv, 0, nullptr, k, topk, topk_scores, ws,
+                        ws_bytes, dev_status);
+}
+
+int dsa_indexer_page_topk(dsa_stream_t stream, const uint16_t* q, const float* w, const uint16_t* kcache,
+                          const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
+                          const int32_t* page_indices, int T, int S, int P, int PTW, int ps, int Hi, int Di,
+                          int max_kv, int k_pages, int32_t* topk_pages, int k, int32_t* topk, float* topk_scores,
+                          void* ws, size_t ws_bytes, int32_t* dev_status) {
+  if (!topk_pages) return DSA_ERR_INVALID_ARGUMENT;
+  return indexer_common(static_cast<cudaStream_t>(stream), q, w, kcache, seq_lens, cu_q_lens, cu_kv_lens,
+                        page_indices, T, S, P, PTW, ps, Hi, Di, max_kv, k_pages, topk_pages, k, topk, topk_scores,
+                        ws, ws_bytes, dev_status);
+}
+
+int dsa_build_block_union(dsa_stream_t stream, const int32_t* topk_units, int T, int K, int QB, int u_max,
+                          const int32_t* cu_q_lens, const int32_t* cu_kv_lens, int S, int ps, int PTW,
+                          int32_t* units, uint32_t* member, int32_t* counts, int32_t* dev_status) {
+  if (T < 0 || K < 1 || QB < 32 || QB % 32 != 0 || QB > 1024 || PTW < 1) return DSA_ERR_INVALID_ARGUMENT;
+  if (cu_q_lens && (!cu_kv_lens || S < 1 || ps < 1)) return DSA_ERR_INVALID_ARGUMENT;
+  if (u_max <= 0) u_max = (int)std::min<long long>((long long)QB * K, PTW);
+  if (T == 0) return DSA_OK;
+  if (!topk_units || !units || !member || !counts) return DSA_ERR_INVALID_ARGUMENT;
+  return run_block_union(static_cast<cudaStream_t>(stream), topk_units, T, K, QB, u_max, cu_q_lens, cu_kv_lens, S,
+                         ps, PTW, units, member, counts, dev_status);
+}
+
+size_t dsa_sparse_mla_decode_workspace_size(int T, int H, int Dv) {
+  if (T <= 0 || H <= 0 || Dv != 512) return 0;
+  const int z = attend_num_splits(T, H, 1 << 30, kModeToken);
+  return attend_workspace_bytes(T, H, z);
+}
+
+int dsa_sparse_mla_decode(dsa_stream_t stream, const uint16_t* q, const uint16_t* kv, int row_stride,
+                          const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
+                          const int32_t* page_indices, const int32_t* sel, int K, int unit, int T, int S, int P,
+                          int PTW, int ps, int H, int Dk, int Dv, float sm_scale, uint16_t* o, float* lse,
+                          void* ws, size_t ws_bytes, int32_t* dev_status) {
+  int rc = check_meta(seq_lens, cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps);
+  if (rc) return rc;
+  rc = attend_check(q, kv, row_stride, T, H, Dk, Dv, o);
+  if (rc) return rc;
+  if (K < 1 || (T > 0 && !sel)) return DSA_ERR_INVALID_ARGUMENT;
+  if (unit != 1 && unit != ps) return DSA_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(sm_scale)) return DSA_ERR_INVALID_ARGUMENT;
+  if (T == 0 || H == 0) return DSA_OK;
+  AttendParams prm{};
+  prm.q = q;
+  prm.kv = kv;
+  prm.row_stride = row_stride;
+  prm.seq_lens = seq_lens;
+  prm.cu_q_lens = cu_q_lens;
+  prm.cu_kv_lens = cu_kv_lens;
+  prm.page_indices = page_indices;
+  prm.T = T;
+  prm.S = S;
+  prm.P = P;
+  prm.PTW = PTW;
+  prm.ps = ps;
+  prm.H = H;
+  prm.scale_log2 = sm_scale * 1.4426950408889634f;
+  prm.mode = unit == 1 ? kModeToken : kModePage;
+  prm.sel = sel;
+  prm.K = K;
+  prm.o = o;
+  prm.lse = lse;
+  prm.dev_status = dev_status;
+  int z = attend_num_splits(T, H, K, prm.mode);
+  if (z > 1 && (!ws || ws_bytes < attend_workspace_bytes(T, H, z) || !aligned16(ws))) z = 1;
+  prm.nsplit = z;
+  return run_attend(static_cast<cudaStream_t>(stream), prm, ws, ws_bytes);
+}
+
+int dsa_sparse_mla_prefill_qblock(dsa_stream_t stream, const uint16_t* q, const uint16_t* kv, int row_stride,
+                                  const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
+                                  const int32_t* page_indices, const int32_t* units, const uint32_t* member,
+                                  const int32_t* counts, int QB, int u_max, int T, int S, int P, int PTW, int ps,
+                                  int H, int Dk, int Dv, float sm_scale, uint16_t* o, float* lse,
+                                  int32_t* dev_status) {
+  int rc = check_meta(seq_lens, cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps);
+  if (rc) return rc;
+  rc = attend_check(q, kv, row_stride, T, H, Dk, Dv, o);
+  if (rc) return rc;
+  if (QB < 32 || QB % 32 != 0 || u_max < 1) return DSA_ERR_INVALID_ARGUMENT;
+  if (T > 0 && (!units || !member || !counts)) return DSA_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(sm_scale)) return DSA_ERR_INVALID_ARGUMENT;
+  if (T == 0 || H == 0) return DSA_OK;
+  AttendParams prm{};
+  prm.q = q;
+  prm.kv = kv;
+  prm.row_stride = row_stride;
+  prm.seq_lens = seq_lens;
+  prm.cu_q_lens = cu_q_lens;
+  prm.cu_kv_lens = cu_kv_lens;
+  prm.page_indices = page_indices;
+  prm.T = T;
+  prm.S = S;
+  prm.P = P;
+  prm.PTW = PTW;
+  prm.ps = ps;
+  prm.H = H;
+  prm.scale_log2 = sm_scale * 1.4426950408889634f;
+  prm.mode = kModeQblock;
+  prm.units = units;
+  prm.member = member;
+  prm.counts = counts;
+  prm.QB = QB;
+  prm.u_max = u_max;
+  prm.K = 1;
+  prm.nsplit = 1;
+  prm.o = o;
+  prm.lse = lse;
+  prm.dev_status = dev_status;
+  return run_attend(static_cast<cudaStream_t>(stream), prm, nullptr, 0);
+}
+
+}  // extern "C"

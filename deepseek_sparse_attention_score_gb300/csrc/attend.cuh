@@ -1,0 +1,44 @@
+// Sparse-MLA attention internals shared by the attention and API units.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+#include <cstddef>
+
+namespace dsa {
+
+enum : int { kModeToken = 0, kModePage = 1, kModeQblock = 2 };
+
+struct AttendParams {
+  const uint16_t* q;   // bf16 [T, H, 576]
+  const uint16_t* kv;  // bf16 [P, ps, row_stride]
+  int row_stride;
+  const int32_t* seq_lens;
+  const int32_t* cu_q_lens;
+  const int32_t* cu_kv_lens;
+  const int32_t* page_indices;
+  int T, S, P, PTW, ps, H;
+  float scale_log2;  // sm_scale * log2(e)
+  int mode;
+  const int32_t* sel;  // token / page modes: [T, K]
+  int K;
+  const int32_t* units;  // qblock mode
+  const uint32_t* member;
+  const int32_t* counts;
+  int QB, u_max;
+  int nsplit;
+  uint16_t* o;      // bf16 [T, H, 512]
+  float* lse;       // [T, H] or null
+  float* o_part;    // [nsplit, T, H, 512] (set by run_attend)
+  float* lse_part;  // [nsplit, T, H]
+  int32_t* dev_status;
+};
+
+int attend_num_splits(int T, int H, int K, int mode);
+size_t attend_workspace_bytes(int T, int H, int nsplit);
+int run_attend(cudaStream_t stream, AttendParams prm, void* ws, size_t ws_bytes);
+
+int run_block_union(cudaStream_t stream, const int32_t* topk_units, int T, int K, int QB, int u_max,
+                    const int32_t* cu_q_lens, const int32_t* cu_kv_lens, int S, int ps, int PTW, int32_t* units,
+                    uint32_t* member, int32_t* counts, int32_t* dev_status);
+
+}  // namespace dsa

@@ -1,0 +1,476 @@
+// Lightning-indexer score on tcgen05 (ref.py, streamindex_topk_ref /
+// streamindex_page_topk_ref: s[t,j] = sum_h relu(q[t,h,:] . k[j,:]) * w[t,h]).
+//
+// Key-major contraction: one UMMA tile is D[128 keys x NQ*32 (query,head)] =
+// K_tile[128 x 128] * Q_tile[NQ*32 x 128]^T, so every TMEM lane holds one key
+// and the ReLU + weighted head sum runs in-thread over its 32 head columns.
+// NQ = 1 serves decode-like tiles (HBM-bound streaming of paged keys), NQ = 8
+// serves prefill tiles (tensor-bound). Keys arrive page by page through 2-D
+// TMA with 128-byte swizzle into a multi-stage ring; the epilogue writes the
+// fp32 token scores and/or the per-page max-pooled scores.
+//
+// A device-side planner turns the ragged metadata into work items
+// (query tile, key chunk) so the persistent kernels never read metadata the
+// host cannot see.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "indexer.cuh"
+
+namespace dsa {
+
+// ------------------------------------------------------------------ planner
+__device__ int block_excl_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int y = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int z = __shfl_up_sync(0xffffffffu, y, o);
+      if (lane >= o) y += z;
+    }
+    s_warp[lane] = y;
+  }
+  __syncthreads();
+  const int excl = x - v + (w > 0 ? s_warp[w - 1] : 0);
+  *total = s_warp[nw - 1];
+  __syncthreads();
+  return excl;
+}
+
+__global__ void __launch_bounds__(1024) indexer_plan_kernel(IndexerMeta m, IndexerPlan pl, int ch1, int ch8) {
+  __shared__ int s_warp[32];
+  const int T = m.T, S = m.S, ps = m.ps;
+  // 1. visible prefix of every token, clamped to the request's page-table span
+  for (int t = threadIdx.x; t < T; t += blockDim.x) {
+    TokenGeom g = token_geom(m.seq_lens, m.cu_q_lens, m.cu_kv_lens, S, ps, m.max_kv, t, m.dev_status);
+    long long cap = (long long)(m.PTW - g.page_base) * ps;
+    int nv = g.n_vis;
+    if (g.page_base < 0 || (long long)nv > cap) {
+      set_status(m.dev_status, DSA_STATUS_BAD_METADATA);
+      nv = cap < 0 || g.page_base < 0 ? 0 : (int)cap;
+    }
+    pl.nvis[t] = nv;
+  }
+  if (threadIdx.x == 0 && (__ldg(m.cu_q_lens) != 0 || __ldg(m.cu_q_lens + S) != T))
+    set_status(m.dev_status, DSA_STATUS_BAD_METADATA);
+  __syncthreads();
+  // 2. per-request tile counts: tiles of up to 8 consecutive tokens; a final
+  //    one-token tile goes to the decode (NQ = 1) list.
+  int carry_d = 0, carry_p = 0;
+  for (int s0 = 0; s0 < S; s0 += blockDim.x) {
+    const int s = s0 + threadIdx.x;
+    int nd = 0, np = 0;
+    if (s < S) {
+      const int ql = __ldg(m.cu_q_lens + s + 1) - __ldg(m.cu_q_lens + s);
+      if (ql > 0) {
+        const int nt = (ql + 7) / 8;
+        nd = (ql - 8 * (nt - 1)) == 1 ? 1 : 0;
+        np = nt - nd;
+      }
+    }
+    int td, tp;
+    const int ed = block_excl_scan(nd, s_warp, &td);
+    const int ep = block_excl_scan(np, s_warp, &tp);
+    if (s < S) pl.seq_tile_off[s] = make_int2(carry_d + ed, carry_p + ep);
+    carry_d += td;
+    carry_p += tp;
+  }
+  __syncthreads();
+  const int n_dec_tiles = carry_d, n_pre_tiles = carry_p;
+  // 3. tile descriptors {first token, ntok, request, visible keys of the last token}
+  for (int t = threadIdx.x; t < T; t += blockDim.x) {
+    const int s = seq_of_token(m.cu_q_lens, S, t);
+    const int q0 = __ldg(m.cu_q_lens + s), ql = __ldg(m.cu_q_lens + s + 1) - q0;
+    const int r = t - q0;
+    if (r % 8) continue;
+    const int ntok = min(8, ql - r);
+    const int nvmax = pl.nvis[t + ntok - 1];
+    const int2 off = pl.seq_tile_off[s];
+    if (ntok == 1) pl.dec_tiles[off.x] = make_int4(t, ntok, s, nvmax);
+    else pl.pre_tiles[off.y + r / 8] = make_int4(t, ntok, s, nvmax);
+  }
+  __syncthreads();
+  // 4. expand tiles into (tile, key chunk) items
+  for (int list = 0; list < 2; ++list) {
+    const int ntiles = list == 0 ? n_dec_tiles : n_pre_tiles;
+    const int4* tiles = list == 0 ? pl.dec_tiles : pl.pre_tiles;
+    int4* items = list == 0 ? pl.dec_items : pl.pre_items;
+    const int ch = list == 0 ? ch1 : ch8;
+    int carry = 0;
+    for (int i0 = 0; i0 < ntiles; i0 += blockDim.x) {
+      const int i = i0 + threadIdx.x;
+      int4 tl = make_int4(0, 0, 0, 0);
+      int n = 0;
+      if (i < ntiles) {
+        tl = tiles[i];
+        n = (tl.w + ch - 1) / ch;
+      }
+      int tot;
+      const int e = block_excl_scan(n, s_warp, &tot);
+      for (int c = 0; c < n; ++c) {
+        const int kb = c * ch, ke = min(tl.w, kb + ch);
+        items[carry + e + c] = make_int4(tl.x, (tl.y << 24) | tl.z, kb, ke);
+      }
+      carry += tot;
+    }
+    if (threadIdx.x == 0) pl.counts[list] = carry;
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------ scorer
+template <int NQ>
+struct IdxCfg {
+  static constexpr int N = NQ * 32;                 // UMMA N: (query, head) columns
+  static constexpr int EPI_WARPS = NQ == 1 ? 4 : 8;  // epilogue warps
+  static constexpr int THREADS = 64 + EPI_WARPS * 32;
+  static constexpr int STAGES = NQ == 1 ? 6 : 3;
+  static constexpr int Q_BYTES = N * 256;            // N rows x 128 dims bf16
+  static constexpr int STAGE_BYTES = 128 * 256;      // 128 keys x 128 dims bf16
+  static constexpr int TMEM_COLS = NQ == 1 ? 64 : 512;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_STAGE = 2 * Q_BYTES;
+  static constexpr int OFF_W = OFF_STAGE + STAGES * STAGE_BYTES;
+  static constexpr int OFF_PMAX = OFF_W + 2 * N * 4;
+  static constexpr int OFF_BAR = OFF_PMAX + 2 * NQ * 4 * 4;
+  static constexpr int NBAR = 2 * STAGES + 9;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 16;
+  static constexpr uint32_t IDESC = make_idesc_bf16(128, N, false, false);
+};
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+template <int NQ>
+__global__ void __launch_bounds__(IdxCfg<NQ>::THREADS, 1)
+    indexer_score_kernel(IndexerMeta m, IndexerPlan pl, IndexerOut out, const __grid_constant__ CUtensorMap kmap,
+                         const __grid_constant__ CUtensorMap qmap) {
+  using C = IdxCfg<NQ>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int n_items = NQ == 1 ? pl.counts[0] : pl.counts[1];
+  if ((int)blockIdx.x >= n_items) return;
+  const int4* items = NQ == 1 ? pl.dec_items : pl.pre_items;
+  if (smem_u32(smem) & 1023u) {  // the swizzled layouts need 1 KB alignment
+    if (threadIdx.x == 0) set_status(m.dev_status, DSA_STATUS_INTERNAL);
+    return;
+  }
+  uint8_t* q_s = smem + C::OFF_Q;
+  uint8_t* st_s = smem + C::OFF_STAGE;
+  float* w_s = reinterpret_cast<float*>(smem + C::OFF_W);
+  float* pmax_s = reinterpret_cast<float*>(smem + C::OFF_PMAX);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::STAGES;
+  uint64_t* qfull = bars + 2 * C::STAGES;
+  uint64_t* qempty = qfull + 2;
+  uint64_t* dfull = qfull + 4;
+  uint64_t* dempty = qfull + 6;
+  uint64_t* fin = qfull + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int warp = warp_id(), lane = lane_id();
+  constexpr int EPI_THREADS = C::EPI_WARPS * 32;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::STAGES; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(qfull + i, 1);
+      mbar_init(qempty + i, 1 + EPI_THREADS);
+      mbar_init(dfull + i, 1);
+      mbar_init(dempty + i, EPI_THREADS);
+    }
+    mbar_init(fin, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tmap(&kmap);
+      prefetch_tmap(&qmap);
+      int kt = 0, it = 0;
+      bool ok = true;
+      for (int ii = blockIdx.x; ii < n_items && ok; ii += gridDim.x, ++it) {
+        const int4 item = items[ii];
+        const int t0 = item.x, ntok = item.y >> 24, seq = item.y & 0xFFFFFF, kb = item.z, ke = item.w;
+        const int qb = it & 1;
+        if (!(ok = mbar_wait(qempty + qb, ((it >> 1) & 1) ^ 1, abort_flag))) break;
+        mbar_arrive_expect_tx(qfull + qb, C::Q_BYTES + ntok * 128);
+        tma_load_2d(q_s + qb * C::Q_BYTES, &qmap, qfull + qb, 0, t0 * 32);
+        tma_load_2d(q_s + qb * C::Q_BYTES + C::N * 128, &qmap, qfull + qb, 64, t0 * 32);
+        bulk_load(w_s + qb * C::N, m.w + (size_t)t0 * 32, ntok * 128, qfull + qb);
+        const int page_base = __ldg(m.cu_kv_lens + seq) / m.ps;
+        const int ppt = 128 / m.ps;  // pages per 128-key tile
+        for (int tile = kb / 128; tile * 128 < ke && ok; ++tile, ++kt) {
+          const int s = kt % C::STAGES;
+          if (!(ok = mbar_wait(empty + s, ((kt / C::STAGES) & 1) ^ 1, abort_flag))) break;
+          int phys[4];
+          int nload = 0;
+          for (int pg = 0; pg < ppt; ++pg) {
+            const int key0 = tile * 128 + pg * m.ps;
+            phys[pg] = -1;
+            if (key0 < ke) {
+              const int p = __ldg(m.page_indices + page_base + key0 / m.ps);
+              if (p >= 0 && p < m.P) {
+                phys[pg] = p;
+                ++nload;
+              } else {
+                set_status(m.dev_status, DSA_STATUS_BAD_METADATA);
+              }
+            }
+          }
+          mbar_arrive_expect_tx(full + s, nload * m.ps * 256);
+          uint8_t* dst = st_s + s * C::STAGE_BYTES;
+          for (int pg = 0; pg < ppt; ++pg) {
+            if (phys[pg] < 0) continue;
+            tma_load_2d(dst + pg * m.ps * 128, &kmap, full + s, 0, phys[pg] * m.ps);
+            tma_load_2d(dst + 16384 + pg * m.ps * 128, &kmap, full + s, 64, phys[pg] * m.ps);
+          }
+        }
+      }
+      // drain: make sure no TMA write is still landing in shared memory
+      for (int d = 1; d <= C::STAGES && d <= kt; ++d) {
+        const int k2 = kt - d;
+        mbar_wait_drain(full + k2 % C::STAGES, (k2 / C::STAGES) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int kt = 0, dt = 0, it = 0;
+      bool ok = true;
+      for (int ii = blockIdx.x; ii < n_items && ok; ii += gridDim.x, ++it) {
+        const int4 item = items[ii];
+        const int kb = item.z, ke = item.w;
+        const int qb = it & 1;
+        if (!(ok = mbar_wait(qfull + qb, (it >> 1) & 1, abort_flag))) break;
+        const uint32_t qaddr = smem_u32(q_s + qb * C::Q_BYTES);
+        for (int tile = kb / 128; tile * 128 < ke; ++tile, ++kt, ++dt) {
+          const int s = kt % C::STAGES, db = dt & 1;
+          if (!(ok = mbar_wait(full + s, (kt / C::STAGES) & 1, abort_flag))) break;
+          if (!(ok = mbar_wait(dempty + db, ((dt >> 1) & 1) ^ 1, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t kaddr = smem_u32(st_s + s * C::STAGE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t a = make_sdesc(kaddr + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+            const uint64_t b = make_sdesc(qaddr + (kk >> 2) * (C::N * 128) + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+            umma_bf16_ss(tmem + db * C::N, a, b, C::IDESC, kk > 0);
+          }
+          umma_commit(empty + s);
+          umma_commit(dfull + db);
+        }
+        if (ok) umma_commit(qempty + qb);
+      }
+      // on an aborted run, wait (bounded) until every issued MMA retired
+      if (!ok && dt > 0) {
+        umma_commit(fin);
+        mbar_wait_drain(fin, 0);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int ew = warp - 2;
+    const int quad = warp & 3;        // TMEM lane quadrant this warp may access
+    const int qset = ew >> 2;         // NQ = 8: queries [4*qset, 4*qset + 4)
+    constexpr int QPW = NQ == 1 ? 1 : 4;
+    const int ps = m.ps;
+    int dt = 0, it = 0;
+    bool ok = true;
+    for (int ii = blockIdx.x; ii < n_items && ok; ii += gridDim.x, ++it) {
+      const int4 item = items[ii];
+      const int t0 = item.x, ntok = item.y >> 24, kb = item.z, ke = item.w;
+      const int qb = it & 1;
+      int nv[QPW];
+#pragma unroll
+      for (int j = 0; j < QPW; ++j) {
+        const int q = qset * 4 + j;
+        nv[j] = q < ntok ? pl.nvis[t0 + q] : 0;
+      }
+      if (!(ok = mbar_wait(qfull + qb, (it >> 1) & 1, abort_flag))) break;
+      const float* wq = w_s + qb * C::N;
+      for (int tile = kb / 128; tile * 128 < ke; ++tile, ++dt) {
+        const int db = dt & 1;
+        if (!(ok = mbar_wait(dfull + db, (dt >> 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        const int key = tile * 128 + quad * 32 + lane;
+#pragma unroll
+        for (int j = 0; j < QPW; ++j) {
+          const int q = qset * 4 + j;
+          if (q >= ntok) break;  // warp-uniform
+          uint32_t r[32];
+          tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + db * C::N + q * 32, r);
+          tmem_ld_wait();
+          float sc = 0.f;
+#pragma unroll
+          for (int h = 0; h < 32; ++h) sc = fmaf(fmaxf(__uint_as_float(r[h]), 0.f), wq[q * 32 + h], sc);
+          const bool valid = key >= kb && key < ke && key < nv[j];
+          if (out.tok_scores && valid) out.tok_scores[(size_t)(t0 + q) * out.ld_tok + key] = sc;
+          if (out.page_scores) {
+            const float pm = warp_max(valid ? sc : -INFINITY);
+            if (ps == 32) {
+              if (lane == 0 && tile * 128 + quad * 32 < nv[j] && tile * 128 + quad * 32 >= kb)
+                out.page_scores[(size_t)(t0 + q) * out.ld_pg + (tile * 128 + quad * 32) / 32] = pm;
+            } else if (lane == 0) {
+              pmax_s[(db * NQ + q) * 4 + quad] = pm;
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(dempty + db);
+        if (out.page_scores && ps > 32) {
+          named_bar_sync(1, EPI_THREADS);
+          // one lane per (query, page of this tile)
+          const int ppt = 128 / ps, qpp = ps / 32;
+          if (ew == 0 && lane < NQ * ppt) {
+            const int q = lane / ppt, pg = lane % ppt;
+            const int key0 = tile * 128 + pg * ps;
+            if (q < ntok) {
+              const int nvq = pl.nvis[t0 + q];
+              if (key0 < nvq && key0 < ke && key0 >= kb) {
+                float pm = -INFINITY;
+                for (int u = 0; u < qpp; ++u) pm = fmaxf(pm, pmax_s[(db * NQ + q) * 4 + pg * qpp + u]);
+                out.page_scores[(size_t)(t0 + q) * out.ld_pg + key0 / ps] = pm;
+              }
+            }
+          }
+        }
+      }
+      if (ok) mbar_arrive(qempty + qb);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    // Normal path: the epilogue consumed every D buffer, so the tensor pipe
+    // is idle. Aborted path: the issuer drained its MMAs above.
+    if (*abort_flag && lane == 0) set_status(m.dev_status, DSA_STATUS_TIMEOUT);
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix with a
+// [64 cols x box_rows] box and 128-byte swizzle.
+static bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = get_encode();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+IndexerLayout indexer_layout(int T, int S, int max_kv, int ps) {
+  IndexerLayout L{};
+  const long long ch1 = kChunkDecode, ch8 = kChunkPrefill;
+  const long long nchunk1 = (max_kv + ch1 - 1) / ch1, nchunk8 = (max_kv + ch8 - 1) / ch8;
+  const long long dec_tiles = S, pre_tiles = (T + 7) / 8 + S;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  L.counts = take(16);
+  L.nvis = take((size_t)T * 4);
+  L.seq_tile_off = take((size_t)S * 8);
+  L.dec_tiles = take((size_t)dec_tiles * 16);
+  L.pre_tiles = take((size_t)pre_tiles * 16);
+  L.dec_items = take((size_t)(dec_tiles * nchunk1) * 16);
+  L.pre_items = take((size_t)(pre_tiles * nchunk8) * 16);
+  L.ld_tok = align_up((size_t)max_kv, 128);
+  L.ld_pg = align_up((size_t)(max_kv + ps - 1) / ps, 4);
+  L.tok_scores = take((size_t)T * L.ld_tok * 4);
+  L.page_scores = take((size_t)T * L.ld_pg * 4);
+  L.total = off;
+  return L;
+}
+
+int run_indexer(cudaStream_t stream, const IndexerMeta& m, const uint16_t* q, const uint16_t* kcache, void* ws,
+                const IndexerLayout& L, bool want_tok, bool want_page, IndexerPlan* plan_out, IndexerOut* out_out) {
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  IndexerPlan pl;
+  pl.counts = reinterpret_cast<int*>(base + L.counts);
+  pl.nvis = reinterpret_cast<int*>(base + L.nvis);
+  pl.seq_tile_off = reinterpret_cast<int2*>(base + L.seq_tile_off);
+  pl.dec_tiles = reinterpret_cast<int4*>(base + L.dec_tiles);
+  pl.pre_tiles = reinterpret_cast<int4*>(base + L.pre_tiles);
+  pl.dec_items = reinterpret_cast<int4*>(base + L.dec_items);
+  pl.pre_items = reinterpret_cast<int4*>(base + L.pre_items);
+  IndexerOut out;
+  out.tok_scores = want_tok ? reinterpret_cast<float*>(base + L.tok_scores) : nullptr;
+  out.page_scores = want_page ? reinterpret_cast<float*>(base + L.page_scores) : nullptr;
+  out.ld_tok = (long long)L.ld_tok;
+  out.ld_pg = (long long)L.ld_pg;
+  *plan_out = pl;
+  *out_out = out;
+  if (m.T == 0) return DSA_OK;
+
+  CUtensorMap kmap, qmap;
+  if (!encode_bf16_2d(&kmap, kcache, (uint64_t)m.P * m.ps, 128, m.ps)) return DSA_ERR_CUDA;
+  if (!encode_bf16_2d(&qmap, q, (uint64_t)m.T * 32, 128, 32)) return DSA_ERR_CUDA;
+  CUtensorMap qmap8;
+  if (!encode_bf16_2d(&qmap8, q, (uint64_t)m.T * 32, 128, 256)) return DSA_ERR_CUDA;
+
+  indexer_plan_kernel<<<1, 1024, 0, stream>>>(m, pl, kChunkDecode, kChunkPrefill);
+  DSA_CHECK_LAUNCH();
+  const int sms = sm_count();
+  {
+    using C = IdxCfg<1>;
+    cudaFuncSetAttribute(indexer_score_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    indexer_score_kernel<1><<<sms, C::THREADS, C::SMEM, stream>>>(m, pl, out, kmap, qmap);
+    DSA_CHECK_LAUNCH();
+  }
+  {
+    using C = IdxCfg<8>;
+    cudaFuncSetAttribute(indexer_score_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    indexer_score_kernel<8><<<sms, C::THREADS, C::SMEM, stream>>>(m, pl, out, kmap, qmap8);
+    DSA_CHECK_LAUNCH();
+  }
+  return DSA_OK;
+}
+
+}  // namespace dsa

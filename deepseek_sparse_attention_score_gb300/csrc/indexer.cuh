@@ -1,0 +1,51 @@
+// Indexer internals shared by the indexer, top-k and API translation units.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+#include <cstddef>
+
+namespace dsa {
+
+constexpr int kChunkDecode = 1024;   // keys per work item of one-token tiles
+constexpr int kChunkPrefill = 2048;  // keys per work item of 8-token tiles
+
+struct IndexerMeta {
+  const float* w;
+  const int32_t* seq_lens;
+  const int32_t* cu_q_lens;
+  const int32_t* cu_kv_lens;
+  const int32_t* page_indices;
+  int T, S, P, PTW, ps, max_kv;
+  int32_t* dev_status;
+};
+
+struct IndexerPlan {
+  int* counts;        // [0] decode items, [1] prefill items
+  int* nvis;          // [T] visible prefix per token
+  int2* seq_tile_off; // [S]
+  int4* dec_tiles;
+  int4* pre_tiles;
+  int4* dec_items;    // {t0, ntok<<24 | seq, key_begin, key_end}
+  int4* pre_items;
+};
+
+struct IndexerOut {
+  float* tok_scores;   // [T, ld_tok] or null
+  float* page_scores;  // [T, ld_pg] or null
+  long long ld_tok, ld_pg;
+};
+
+struct IndexerLayout {
+  size_t counts, nvis, seq_tile_off, dec_tiles, pre_tiles, dec_items, pre_items, tok_scores, page_scores;
+  size_t ld_tok, ld_pg, total;
+};
+
+IndexerLayout indexer_layout(int T, int S, int max_kv, int ps);
+int run_indexer(cudaStream_t stream, const IndexerMeta& m, const uint16_t* q, const uint16_t* kcache, void* ws,
+                const IndexerLayout& L, bool want_tok, bool want_page, IndexerPlan* plan_out, IndexerOut* out_out);
+
+// Exact per-row top-k over a score buffer (token or page scores).
+int run_topk(cudaStream_t stream, const float* scores, long long ld, const int* nvis, int T, int div, int k,
+             int32_t* out_idx, float* out_val, int max_len);
+
+}  // namespace dsa

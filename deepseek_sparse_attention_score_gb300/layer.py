@@ -1,0 +1,109 @@
+"""One DSA layer step on a resident batch, built from the C-ABI calls.
+
+Decode batches run indexer -> token top-k (or page top-k with a page budget)
+-> sparse MLA decode. Prefill / mixed batches run, on full layers, the
+indexer once for both the page top-k (K_p = ceil(k/ps), what the attention
+consumes) and the token top-k, then the block union and the query-block
+sparse MLA; shared layers (IndexShare, ref.py build_index_share_map) reuse the
+top-k and union tables of their source slot and run the attention only.
+
+All buffers are allocated once up front, so a step only enqueues kernels and
+can be captured in a CUDA graph.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import abi
+
+
+class LayerRunner:
+    def __init__(self, wl, device, page_budget=None, prefill=None):
+        """``wl``: a dsa_inputs.Workload whose tensors already live on ``device``
+        (or on the CPU; they are moved). ``page_budget``: decode page-budget
+        mode with that many pages. ``prefill``: force the prefill path
+        (default: any request with more than one new token)."""
+        rg = wl.rg
+        self.wl = wl
+        self.dev = torch.device(device)
+        dev = self.dev
+        self.rg = rg
+        self.T, self.S, self.P, self.PTW, self.ps = rg.T, rg.S, rg.num_pages, rg.PTW, rg.page_size
+        self.max_kv = max(1, rg.max_kv)
+        self.k = wl.k
+        self.k_pages = wl.k_pages if page_budget is None else page_budget
+        self.page_budget = page_budget
+        self.prefill = bool((rg.q_lens > 1).any()) if prefill is None else prefill
+        to = lambda a: torch.from_numpy(a).to(dev)
+        self.meta = [to(rg.seq_lens), to(rg.cu_q_lens), to(rg.cu_kv_lens), to(rg.page_indices)]
+        self.q_idx = wl.q_idx.to(dev)
+        self.w = wl.w.to(dev)
+        self.kcache = [c.to(dev) for c in wl.kcache]
+        self.q = [x.to(dev) for x in wl.q]
+        self.kv = [x.to(dev) for x in wl.kv]
+        self.types = list(wl.indexer_types) if wl.indexer_types else [0]
+        self.full_slot, self.src_slot, self.num_full = abi.dsa_index_build_share_map(self.types, len(self.types))
+        T, H = self.T, wl.H
+        self.H = H
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.ws_idx = torch.empty(max(1, abi.dsa_indexer_workspace_size(T, self.S, self.max_kv, self.ps)),
+                                  dtype=torch.uint8, device=dev)
+        self.ws_att = torch.empty(max(1, abi.dsa_sparse_mla_decode_workspace_size(T, H)), dtype=torch.uint8,
+                                  device=dev)
+        nl = len(self.types)
+        self.topk = [torch.empty((T, self.k), dtype=torch.int32, device=dev) for _ in range(self.num_full)]
+        self.topk_pages = [torch.empty((T, self.k_pages), dtype=torch.int32, device=dev)
+                           for _ in range(self.num_full)]
+        self.o = [torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev) for _ in range(nl)]
+        if self.prefill:
+            self.QB = wl.QB
+            self.u_max = wl.u_max if wl.u_max > 0 else min(self.QB * self.k_pages, self.PTW)
+            nqb = (T + self.QB - 1) // self.QB
+            self.units = [torch.empty((nqb, self.u_max), dtype=torch.int32, device=dev) for _ in range(self.num_full)]
+            self.member = [torch.empty((nqb, self.u_max, self.QB // 32), dtype=torch.int32, device=dev)
+                           for _ in range(self.num_full)]
+            self.counts = [torch.empty((nqb,), dtype=torch.int32, device=dev) for _ in range(self.num_full)]
+
+    # -- stages ---------------------------------------------------------------
+    def index(self, slot):
+        if self.prefill or self.page_budget is not None:
+            abi.dsa_indexer_page_topk(self.q_idx, self.w, self.kcache[slot], *self.meta, k_pages=self.k_pages,
+                                      max_kv=self.max_kv, topk_pages=self.topk_pages[slot], k=self.k,
+                                      topk=self.topk[slot] if self.prefill else None, ws=self.ws_idx,
+                                      dev_status=self.status)
+        else:
+            abi.dsa_indexer_topk(self.q_idx, self.w, self.kcache[slot], *self.meta, k=self.k, max_kv=self.max_kv,
+                                 topk=self.topk[slot], ws=self.ws_idx, dev_status=self.status)
+
+    def union(self, slot):
+        abi.dsa_build_block_union(self.topk_pages[slot], QB=self.QB, u_max=self.u_max, cu_q_lens=self.meta[1],
+                                  cu_kv_lens=self.meta[2], ps=self.ps, PTW=self.PTW, units=self.units[slot],
+                                  member=self.member[slot], counts=self.counts[slot], dev_status=self.status)
+
+    def attend(self, layer):
+        slot = self.src_slot[layer]
+        if self.prefill:
+            abi.dsa_sparse_mla_prefill_qblock(self.q[layer], self.kv[layer], *self.meta, self.units[slot],
+                                              self.member[slot], self.counts[slot], QB=self.QB,
+                                              sm_scale=self.wl.sm_scale, o=self.o[layer], dev_status=self.status)
+        elif self.page_budget is not None:
+            abi.dsa_sparse_mla_decode(self.q[layer], self.kv[layer], *self.meta, self.topk_pages[slot],
+                                      unit=self.ps, sm_scale=self.wl.sm_scale, o=self.o[layer], ws=self.ws_att,
+                                      dev_status=self.status)
+        else:
+            abi.dsa_sparse_mla_decode(self.q[layer], self.kv[layer], *self.meta, self.topk[slot], unit=1,
+                                      sm_scale=self.wl.sm_scale, o=self.o[layer], ws=self.ws_att,
+                                      dev_status=self.status)
+
+    def layer_step(self, layer):
+        if self.full_slot[layer] >= 0:
+            slot = self.full_slot[layer]
+            self.index(slot)
+            if self.prefill:
+                self.union(slot)
+        self.attend(layer)
+
+    def step(self):
+        """Every layer of the workload once (IndexShare across layers)."""
+        for layer in range(len(self.types)):
+            self.layer_step(layer)

@@ -1,0 +1,213 @@
+/*
+ * dsa.h - C ABI of the GB300 (sm_103a) DeepSeek-Sparse-Attention hot path.
+ *
+ * The operations follow the sglang-jax DSA pages:
+ *   "ref.py" (jnp reference implementations): build_index_share_map,
+ *       streamindex_topk_ref, streamindex_page_topk_ref, sparse_mla_ref;
+ *   "sparse_mla_prefill_qblock.py" (blocked sparse-MLA prefill):
+ *       build_block_unit_tables, _qblock_kernel, sparse_mla_attention_qblock;
+ *   "dsa_sparse_backend.py" (DSA sparse attention backend): IndexShare and the
+ *       page budgets.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.   Every tensor pointer is a DEVICE pointer owned by the caller,
+ *           except where an argument is marked "host". The library allocates
+ *           no memory: scratch space is a caller-provided workspace whose size
+ *           the matching *_workspace_size() call reports.
+ * Streams.  Every device entry point only enqueues kernels on `stream` (a
+ *           cudaStream_t; NULL is the legacy default stream) and never
+ *           synchronises, so calls may be captured in a CUDA graph.
+ * dtypes.   bf16 tensors are passed as uint16_t (the raw bit pattern);
+ *           metadata is int32.
+ * Ragged batch metadata (identical for all calls, "D4" of the pages):
+ *   seq_lens     [S]    kv length of request s, INCLUDING its new tokens;
+ *   cu_q_lens    [S+1]  query-token offsets (cu_q_lens[S] == T);
+ *   cu_kv_lens   [S+1]  cumulative page-aligned kv lengths; request s owns the
+ *                       packed page-table entries starting at cu_kv_lens[s]/ps;
+ *   page_indices [PTW]  physical page of every packed page-table entry, < P.
+ *   Query token t of request s sits at absolute position
+ *   pos(t) = seq_lens[s] - q_len(s) + (t - cu_q_lens[s]); it sees the key
+ *   positions j with j < seq_lens[s] and j <= pos(t) (causal + kv_len mask).
+ * Padding.  Unused index slots are -1. Selected sets are written in
+ *           ascending index order.
+ * Status.   Host-detected errors return a negative DSA_ERR_* code and enqueue
+ *           nothing. Conditions detected on the device are OR-ed into the
+ *           optional `dev_status` word (device int32, may be NULL): the
+ *           offending access is skipped, never trapped.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define DSA_API __attribute__((visibility("default")))
+#else
+#define DSA_API
+#endif
+
+typedef void* dsa_stream_t; /* a cudaStream_t */
+
+enum dsa_error {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARGUMENT = -1, /* null pointer, negative size, T != ... */
+  DSA_ERR_UNSUPPORTED = -2,      /* a shape this build does not implement */
+  DSA_ERR_WORKSPACE = -3,        /* workspace missing or too small */
+  DSA_ERR_CUDA = -4,             /* a CUDA call or kernel launch failed */
+  DSA_ERR_SHARED_BEFORE_FULL = -5,
+  DSA_ERR_BAD_INDEXER_TYPE = -6,
+  DSA_ERR_ALIGNMENT = -7 /* a pointer is not 16-byte aligned */
+};
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define DSA_STATUS_UNION_TRUNCATED 0x1 /* a block's union exceeded u_max */
+#define DSA_STATUS_BAD_METADATA 0x2    /* ragged metadata out of range */
+#define DSA_STATUS_BAD_INDEX 0x4       /* a selected unit or page id out of range */
+#define DSA_STATUS_TIMEOUT 0x8         /* a pipeline wait gave up (about 2 s) */
+#define DSA_STATUS_INTERNAL 0x10       /* a launch-time invariant failed on the device */
+
+/* ------------------------------------------------------------------------
+ * IndexShare layer -> slot map (host only).
+ * ref.py, build_index_share_map: a full layer (type 0) opens a new indexer
+ * slot; a shared layer (type 1) consumes the slot of the nearest preceding
+ * full layer and runs no indexer. types == NULL means every layer is full.
+ * skip_offset is accepted and ignored, as on the page.
+ *   types      host int32 [num_layers] (0 = full, 1 = shared) or NULL
+ *   full_slot  host int32 [num_layers] out: slot of a full layer, -1 otherwise
+ *   src_slot   host int32 [num_layers] out: slot whose top-k the layer uses
+ *   num_full   host int32 out: number of full layers (= indexer key caches)
+ * Errors: DSA_ERR_SHARED_BEFORE_FULL, DSA_ERR_BAD_INDEXER_TYPE.
+ * ------------------------------------------------------------------------ */
+DSA_API int dsa_index_build_share_map(const int32_t* types, int num_layers, int skip_offset, int32_t* full_slot,
+                              int32_t* src_slot, int32_t* num_full);
+
+/* ------------------------------------------------------------------------
+ * Lightning indexer + exact token top-k.
+ * ref.py, streamindex_topk_ref: s[t,j] = sum_h relu(q[t,h,:] . k[j,:]) * w[t,h]
+ * accumulated in fp32 over the visible prefix j < min(seq_lens[s], pos(t)+1);
+ * then the k highest-scoring visible positions, ties to the lower index
+ * (exact: the pages' approximate top-k is not used).
+ *   q        bf16 [T, Hi, Di]       indexer queries
+ *   w        fp32 [T, Hi]           head weights (any scale folded in)
+ *   kcache   bf16 [P, ps, Di]       paged indexer keys
+ *   max_kv   upper bound of seq_lens (sizes the score workspace); a larger
+ *            seq_len is clamped and flagged DSA_STATUS_BAD_METADATA
+ *   topk     int32 [T, k] out       ascending positions, -1 padded
+ *   topk_scores fp32 [T, k] out or NULL: the scores of `topk` (-inf on pads)
+ *   ws/ws_bytes  workspace of dsa_indexer_workspace_size(T, S, max_kv, ps) bytes
+ * Supported: Hi == 32, Di == 128, ps in {32, 64, 128}, 1 <= k.
+ * ------------------------------------------------------------------------ */
+DSA_API size_t dsa_indexer_workspace_size(int T, int S, int max_kv, int ps);
+DSA_API int dsa_indexer_topk(dsa_stream_t stream, const uint16_t* q, const float* w, const uint16_t* kcache,
+                     const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
+                     const int32_t* page_indices, int T, int S, int P, int PTW, int ps, int Hi, int Di, int max_kv,
+                     int k, int32_t* topk, float* topk_scores, void* ws, size_t ws_bytes, int32_t* dev_status);
+
+/* ------------------------------------------------------------------------
+ * Lightning indexer + page top-k (and, optionally, the token top-k from the
+ * same score pass).
+ * ref.py, streamindex_page_topk_ref: the token scores are max-pooled per page
+ * of ps positions (masked positions excluded), then the k_pages best pages
+ * are kept (ties to the lower page); pages with no visible position are never
+ * selected. Page ids are sequence-local; unused slots are -1.
+ * The prefill budget of dsa_sparse_backend.py is k_pages = ceil(k / ps); the
+ * decode page budget is min(budget, pages_per_seq).
+ *   topk_pages  int32 [T, k_pages] out
+ *   k, topk, topk_scores  as dsa_indexer_topk; topk == NULL skips the token
+ *               top-k (k is then ignored).
+ * ------------------------------------------------------------------------ */
+DSA_API int dsa_indexer_page_topk(dsa_stream_t stream, const uint16_t* q, const float* w, const uint16_t* kcache,
+                          const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
+                          const int32_t* page_indices, int T, int S, int P, int PTW, int ps, int Hi, int Di,
+                          int max_kv, int k_pages, int32_t* topk_pages, int k, int32_t* topk, float* topk_scores,
+                          void* ws, size_t ws_bytes, int32_t* dev_status);
+
+/* ------------------------------------------------------------------------
+ * Per-query-block union of selected units and the membership bitmap.
+ * sparse_mla_prefill_qblock.py, build_block_unit_tables (plus the lift of
+ * sparse_mla_attention_qblock's ragged mode): token t's sequence-local page
+ * ids p >= 0 become global page-table keys g = cu_kv_lens[seq(t)]/ps + p
+ * (cu_q_lens == NULL: ids are already global). T is padded to a multiple of
+ * QB with empty rows. For block b:
+ *   units   int32 [nQB, u_max]        ascending unique ids, -1 padded; a union
+ *                                      larger than u_max keeps its u_max
+ *                                      smallest ids and sets
+ *                                      DSA_STATUS_UNION_TRUNCATED
+ *   member  uint32 [nQB, u_max, QB/32] bit (q % 32) of word q/32 of slot u is
+ *                                      1 iff query q of the block selected
+ *                                      units[b, u] (slot-major, bit-packed)
+ *   counts  int32 [nQB]               true (uncapped) union size
+ * with nQB = ceil(T / QB). u_max <= 0 selects the lossless bound
+ * min(QB * K, PTW); the outputs must then be sized with that value.
+ *   topk_units int32 [T, K]  selected units per query, -1 padded
+ * Supported: QB % 32 == 0, QB <= 1024. Needs no workspace.
+ * ------------------------------------------------------------------------ */
+DSA_API int dsa_build_block_union(dsa_stream_t stream, const int32_t* topk_units, int T, int K, int QB, int u_max,
+                          const int32_t* cu_q_lens, const int32_t* cu_kv_lens, int S, int ps, int PTW,
+                          int32_t* units, uint32_t* member, int32_t* counts, int32_t* dev_status);
+
+/* ------------------------------------------------------------------------
+ * Sparse absorbed-MLA attention over per-query selections (decode form).
+ * ref.py, sparse_mla_ref: for query t and head h,
+ *   o[t,h,:] = sum_j softmax_j(sm_scale * q[t,h,:Dk] . kv[j,:Dk]) kv[j,:Dv]
+ * over the selected positions j that are visible (j < seq_len, j <= pos(t));
+ * the value is the first Dv columns of the same latent row. A query with no
+ * visible selected key outputs 0 (lse = -inf). Logits and softmax in fp32,
+ * output rounded to bf16.
+ *   q      bf16 [T, H, Dk]               [q_nope | q_rope]
+ *   kv     bf16 [P, ps, row_stride]      [c_kv(Dv) | k_rope | pad]
+ *   sel    int32 [T, K]  unit == 1: token positions; unit == ps: sequence-
+ *                        local page ids (each expands to ps positions);
+ *                        -1 entries are ignored, order does not matter
+ *   o      bf16 [T, H, Dv] out
+ *   lse    fp32 [T, H] out or NULL: natural-log sum of exp of the logits
+ *   ws     workspace of dsa_sparse_mla_decode_workspace_size(T, H, Dv) bytes
+ *          (split-key partials; 0 bytes needed when T*H is large)
+ * Supported: Dk == 576, Dv == 512, row_stride in {576, 640}, ps in
+ * {32, 64, 128}, H >= 1 (heads are processed 128 at a time).
+ * ------------------------------------------------------------------------ */
+DSA_API size_t dsa_sparse_mla_decode_workspace_size(int T, int H, int Dv);
+DSA_API int dsa_sparse_mla_decode(dsa_stream_t stream, const uint16_t* q, const uint16_t* kv, int row_stride,
+                          const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
+                          const int32_t* page_indices, const int32_t* sel, int K, int unit, int T, int S, int P,
+                          int PTW, int ps, int H, int Dk, int Dv, float sm_scale, uint16_t* o, float* lse,
+                          void* ws, size_t ws_bytes, int32_t* dev_status);
+
+/* ------------------------------------------------------------------------
+ * Query-block sparse-MLA prefill over the block unions.
+ * sparse_mla_prefill_qblock.py, _qblock_kernel / sparse_mla_attention_qblock:
+ * query t of block b = t / QB walks the slots u < min(counts[b], u_max) of its
+ * block; unit g = units[b,u] is physical page page_indices[g] whose row r is
+ * key position kp = g*ps + r - (cu_kv_lens[seq(t)]/ps)*ps, visible iff the
+ * membership bit of (u, t % QB) is set and kp <= pos(t) and kp < seq_len.
+ * Same masked-softmax math and output as dsa_sparse_mla_decode with page
+ * units (the pages' parity claim between the blocked and per-query kernels).
+ *   units/member/counts  as written by dsa_build_block_union (same QB, u_max)
+ *   o      bf16 [T, H, Dv] out; lse fp32 [T, H] out or NULL
+ * Supported: as dsa_sparse_mla_decode. Needs no workspace.
+ * ------------------------------------------------------------------------ */
+DSA_API int dsa_sparse_mla_prefill_qblock(dsa_stream_t stream, const uint16_t* q, const uint16_t* kv, int row_stride,
+                                  const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
+                                  const int32_t* page_indices, const int32_t* units, const uint32_t* member,
+                                  const int32_t* counts, int QB, int u_max, int T, int S, int P, int PTW, int ps,
+                                  int H, int Dk, int Dv, float sm_scale, uint16_t* o, float* lse,
+                                  int32_t* dev_status);
+
+/* Number of streaming multiprocessors the kernels size their grids for
+ * (device of the current context); a query helper, no device work. */
+DSA_API int dsa_device_sm_count(void);
+
+/* Number of kernels this process has enqueued through the library so far
+ * (a host-side counter; a diagnostic, no device work). */
+DSA_API long long dsa_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSA_H_ */
