@@ -10,9 +10,13 @@
 // room for S, so the value width is split across two CTAs that both form S
 // (the pair reads the same keys; the second read is an L2 hit).
 //
-// Keys are gathered row by row (1152 bytes each) with cp.async into a
-// two-stage ring laid out as 128-byte-swizzled column blocks; the same bytes
-// serve as the K-major B operand of QK^T and as the MN-major B operand of PV.
+// Q[:, 0:448] is kept in TMEM and feeds QK^T as the A operand (tcgen05 "TS"
+// form), which keeps shared memory free for five KV stages and removes most
+// of the A-operand shared-memory traffic; Q[:, 448:576] stays in shared
+// memory. Keys are gathered row by row (1152 bytes each) with cp.async into
+// the ring of 128-byte-swizzled column blocks; the same bytes serve as the
+// K-major B operand of QK^T and as the MN-major B operand of PV. One warp
+// walks the key list ahead of the gather and prefetches the rows into L2.
 // Key lists come from (a) token top-k rows, (b) page top-k rows, or (c) a
 // query block's union + membership bitmap (qblock form). Masked keys are
 // zero-filled and get probability 0.
@@ -22,26 +26,33 @@
 namespace dsa {
 
 namespace {
-constexpr int kThreads = 256;        // warp 0 MMA, warps 1-3 gather, warps 4-7 softmax
-constexpr int kProdThreads = 96;
+constexpr int kThreads = 256;  // warp 0 MMA, warp 1 key generator, warps 2-3 gather, warps 4-7 softmax
+constexpr int kCopyThreads = 64;
 constexpr int kTileKeys = 32;
+constexpr int kStages = 5;   // KV tiles resident in shared memory
+constexpr int kRing = 8;     // key-address tiles generated (and L2-prefetched) ahead of the gather
 constexpr int kDk = 576, kDv = 512, kDvHalf = 256;
-constexpr int kQBytes = 128 * kDk * 2;              // 147456: 9 column blocks x 16 KB
-constexpr int kStageBytes = kTileKeys * kDk * 2;    // 36864: 9 column blocks x 4 KB
-constexpr int kPBytes = 128 * kTileKeys * 2;        // 8192
-constexpr int OFF_Q = 0;
-constexpr int OFF_ST = OFF_Q + kQBytes;
-constexpr int OFF_P = OFF_ST + 2 * kStageBytes;
-constexpr int OFF_ROWS = OFF_P + kPBytes;           // int32 [2][32]
-constexpr int OFF_INFO = OFF_ROWS + 2 * 32 * 4;     // uint32 mask[2], end[2]
-constexpr int OFF_BAR = OFF_INFO + 16;
-constexpr int NBAR = 11;
+constexpr int kQTmemDims = 448;  // Q[:, 0:448] lives in TMEM (224 columns), Q[:, 448:576] in smem
+constexpr int kQTmemSteps = kQTmemDims / 16;  // 28 of the 36 K-steps read A from TMEM
+constexpr int kQsBytes = 128 * (kDk - kQTmemDims) * 2;  // 32768: 2 column blocks x 16 KB
+constexpr int kStageBytes = kTileKeys * kDk * 2;        // 36864: 9 column blocks x 4 KB
+constexpr int kPBytes = 128 * kTileKeys * 2;            // 8192
+constexpr int OFF_QS = 0;
+constexpr int OFF_ST = OFF_QS + kQsBytes;
+constexpr int OFF_P = OFF_ST + kStages * kStageBytes;
+constexpr int OFF_RING = OFF_P + kPBytes;         // int32 [kRing][32] physical rows
+constexpr int OFF_RINFO = OFF_RING + kRing * 32 * 4;  // uint32 mask[kRing], end[kRing]
+constexpr int OFF_SINFO = OFF_RINFO + kRing * 8;      // uint32 mask[kStages], end[kStages]
+constexpr int OFF_BAR = (OFF_SINFO + kStages * 8 + 7) & ~7;
+constexpr int NBAR = 2 * kStages + 2 * kRing + 5;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int kSmem = OFF_MISC + 16;
 constexpr uint32_t kIdescQK = make_idesc_bf16(128, kTileKeys, false, false);
 constexpr uint32_t kIdescPV = make_idesc_bf16(128, kDvHalf, false, true);
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kColQ = 0;    // 224 columns of packed bf16 pairs
+constexpr uint32_t kColS = 224;  // 32 fp32 columns
+constexpr uint32_t kColO = 256;  // 256 fp32 columns
 constexpr float kRescaleThreshold = 8.f;  // log2 units: p stays <= 256
 }  // namespace
 
@@ -199,79 +210,114 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const AttendPar
   const int half = blockIdx.x & 1, hg = blockIdx.x >> 1;
   const int t = blockIdx.y, split = blockIdx.z;
   const int h0 = hg * 128;
-  uint8_t* q_s = smem + OFF_Q;
+  uint8_t* qs_s = smem + OFF_QS;
   uint8_t* st_s = smem + OFF_ST;
   uint8_t* p_s = smem + OFF_P;
-  int* rows_s = reinterpret_cast<int*>(smem + OFF_ROWS);
-  volatile uint32_t* info_mask = reinterpret_cast<volatile uint32_t*>(smem + OFF_INFO);
-  volatile uint32_t* info_end = info_mask + 2;
+  int* ring_rows = reinterpret_cast<int*>(smem + OFF_RING);
+  volatile uint32_t* ring_mask = reinterpret_cast<volatile uint32_t*>(smem + OFF_RINFO);
+  volatile uint32_t* ring_end = ring_mask + kRing;
+  volatile uint32_t* st_mask = reinterpret_cast<volatile uint32_t*>(smem + OFF_SINFO);
+  volatile uint32_t* st_end = st_mask + kStages;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint64_t* full = bars;        // [2] 96 gather threads
-  uint64_t* empty = bars + 2;   // [2] PV commit
-  uint64_t* sfull = bars + 4;   // [2] QK commit
-  uint64_t* sempty = bars + 6;  // [2] 128 softmax threads
-  uint64_t* pfull = bars + 8;   // 128 softmax threads
-  uint64_t* pempty = bars + 9;  // PV commit
-  uint64_t* fin = bars + 10;
+  uint64_t* full = bars;                  // [kStages] 64 async + 1 leader arrivals
+  uint64_t* empty = bars + kStages;       // [kStages] PV commit
+  uint64_t* rfull = bars + 2 * kStages;   // [kRing] generator
+  uint64_t* rempty = rfull + kRing;       // [kRing] 64 gather threads
+  uint64_t* sfull = rempty + kRing;       // QK commit
+  uint64_t* sempty = sfull + 1;           // 128 softmax threads
+  uint64_t* pfull = sfull + 2;            // 128 softmax threads
+  uint64_t* pempty = sfull + 3;           // PV commit
+  uint64_t* fin = sfull + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(full + i, kProdThreads);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(full + i, kCopyThreads + 1);
       mbar_init(empty + i, 1);
-      mbar_init(sfull + i, 1);
-      mbar_init(sempty + i, 128);
     }
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(rfull + i, 1);
+      mbar_init(rempty + i, kCopyThreads);
+    }
+    mbar_init(sfull, 1);
+    mbar_init(sempty, 128);
     mbar_init(pfull, 128);
     mbar_init(pempty, 1);
     mbar_init(fin, 1);
     *abort_flag = 0;
-    info_end[0] = 0;
-    info_end[1] = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  // Q tile [128 heads x 576] -> nine 128-byte-swizzled column blocks
+  const int nh = min(128, prm.H - h0);
+  const uint16_t* qt = prm.q + ((size_t)t * prm.H + h0) * kDk;
+  // Q[:, 448:576] -> two 128-byte-swizzled column blocks in shared memory
   {
-    const int nh = min(128, prm.H - h0);
-    const uint16_t* qt = prm.q + ((size_t)t * prm.H + h0) * kDk;
-    const uint32_t qbase = smem_u32(q_s);
-    for (int c = tid; c < 128 * 72; c += kThreads) {
-      const int r = c / 72, ch = c % 72;
+    const uint32_t qbase = smem_u32(qs_s);
+    constexpr int CH = (kDk - kQTmemDims) / 8;  // 16 chunks of 16 bytes per row
+    for (int c = tid; c < 128 * CH; c += kThreads) {
+      const int r = c / CH, ch = c % CH;
       const bool ok = r < nh;
-      const uint16_t* src = ok ? qt + (size_t)r * kDk + ch * 8 : prm.q;
+      const uint16_t* src = ok ? qt + (size_t)r * kDk + kQTmemDims + ch * 8 : prm.q;
       cp_async16(qbase + (ch >> 3) * 16384 + sw128_offset(r, ch & 7), src, ok ? 16u : 0u);
     }
     cp_async_commit();
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (warp >= 4) {
+    // Q[:, 0:448] -> TMEM lanes (one head row per lane), bf16 pairs per column
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint4* src = reinterpret_cast<const uint4*>(qt + (size_t)r * kDk);
+#pragma unroll 1
+    for (int c0 = 0; c0 < kQTmemDims / 2; c0 += 32) {
+      uint32_t v[32];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint4 x = r < nh ? __ldg(src + c0 / 4 + j) : make_uint4(0, 0, 0, 0);
+        v[4 * j] = x.x;
+        v[4 * j + 1] = x.y;
+        v[4 * j + 2] = x.z;
+        v[4 * j + 3] = x.w;
+      }
+      tmem_st32(tmem + lane_base + kColQ + c0, v);
+    }
+    tmem_st_wait();
+  }
+  cp_async_wait<0>();
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 
   if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t qaddr = smem_u32(q_s), paddr = smem_u32(p_s);
+      const uint32_t qsaddr = smem_u32(qs_s), paddr = smem_u32(p_s);
       auto issue_qk = [&](int i) {
-        const int s = i & 1;
-        const uint32_t kaddr = smem_u32(st_s + s * kStageBytes);
+        const uint32_t kaddr = smem_u32(st_s + (i % kStages) * kStageBytes);
 #pragma unroll 4
-        for (int kk = 0; kk < kDk / 16; ++kk) {
-          const uint64_t a = make_sdesc(qaddr + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+        for (int kk = 0; kk < kQTmemSteps; ++kk) {
           const uint64_t b = make_sdesc(kaddr + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
-          umma_bf16_ss(tmem + s * kTileKeys, a, b, kIdescQK, kk > 0);
+          umma_bf16_ts(tmem + kColS, tmem + kColQ + kk * 8, b, kIdescQK, kk > 0);
         }
-        umma_commit(sfull + s);
+#pragma unroll
+        for (int kk = kQTmemSteps; kk < kDk / 16; ++kk) {
+          const int k2 = kk - kQTmemSteps;
+          const uint64_t a = make_sdesc(qsaddr + (k2 >> 2) * 16384 + (k2 & 3) * 32, 16, 1024, kSwizzle128B);
+          const uint64_t b = make_sdesc(kaddr + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+          umma_bf16_ss(tmem + kColS, a, b, kIdescQK, 1u);
+        }
+        umma_commit(sfull);
       };
       auto issue_pv = [&](int i) {
-        const int s = i & 1;
+        const int s = i % kStages;
         const uint32_t vaddr = smem_u32(st_s + s * kStageBytes) + half * 4 * 4096;
 #pragma unroll
         for (int ks = 0; ks < kTileKeys / 16; ++ks) {
@@ -284,16 +330,19 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const AttendPar
       };
       bool ok = mbar_wait(full + 0, 0, abort_flag);
       int issued = 0;
-      if (ok && !info_end[0]) {
+      if (ok && !st_end[0]) {
+        fence_proxy_async_smem();  // cp.async data -> async proxy
         tc_fence_after();
         issue_qk(0);
         issued = 1;
         for (int i = 0;; ++i) {
-          const int s1 = (i + 1) & 1;
-          if (!(ok = mbar_wait(full + s1, ((i + 1) >> 1) & 1, abort_flag))) break;
-          const bool end1 = info_end[s1] != 0;
+          const int s1 = (i + 1) % kStages;
+          if (!(ok = mbar_wait(full + s1, ((i + 1) / kStages) & 1, abort_flag))) break;
+          const bool end1 = st_end[s1] != 0;
           if (!end1) {
-            if (!(ok = mbar_wait(sempty + s1, (((i + 1) >> 1) & 1) ^ 1, abort_flag))) break;
+            fence_proxy_async_smem();
+            // single S buffer: softmax must have read S(i)
+            if (!(ok = mbar_wait(sempty, i & 1, abort_flag))) break;
             tc_fence_after();
             issue_qk(i + 1);
           }
@@ -308,57 +357,58 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const AttendPar
         mbar_wait_drain(fin, 0);
       }
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------ gather
-    const int ptid = tid - 32;
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ key generator + L2 prefetch
     TileGen gen;
-    if (warp == 1) gen.init(prm, t, split);
-    const uint32_t stbase = smem_u32(st_s);
-    int i = 0;
-    bool ok = true;
-    while (true) {
+    gen.init(prm, t, split);
+    for (int j = 0;; ++j) {
       long long row = -1;
       uint32_t mask = 0;
-      bool more = false;
-      if (warp == 1) more = gen.next(row, mask);
-      const int s = i & 1;
-      if (warp == 1) {
-        if (lane == 0) ok = mbar_wait(empty + s, ((i >> 1) & 1) ^ 1, abort_flag);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (ok) {
-          // rows are < 2^31 for any pool this ABI can describe (P * ps int)
-          rows_s[s * 32 + lane] = (int)row;
-          if (lane == 0) {
-            info_mask[s] = mask;
-            info_end[s] = more ? 0u : 1u;
-          }
-        } else if (lane == 0) {
-          info_end[s] = 1u;
-        }
+      const bool more = gen.next(row, mask);
+      const int slot = j % kRing;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(rempty + slot, ((j / kRing) & 1) ^ 1, abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      ring_rows[slot * 32 + lane] = more ? (int)row : -1;
+      if (more && row >= 0) prefetch_l2_bulk(prm.kv + (size_t)row * prm.row_stride, kDk * 2);
+      if (lane == 0) {
+        ring_mask[slot] = mask;
+        ring_end[slot] = more ? 0u : 1u;
       }
-      named_bar_sync(1, kProdThreads);
-      if (!ok || *abort_flag) break;
-      const bool end = info_end[s] != 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(rfull + slot);
+      if (!more) break;
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ gather
+    const int ctid = tid - 64;
+    const uint32_t stbase = smem_u32(st_s);
+    for (int i = 0;; ++i) {
+      const int slot = i % kRing, s = i % kStages;
+      if (!mbar_wait(rfull + slot, (i / kRing) & 1, abort_flag)) break;
+      const bool end = ring_end[slot] != 0;
+      const uint32_t mask = ring_mask[slot];
+      if (!mbar_wait(empty + s, ((i / kStages) & 1) ^ 1, abort_flag)) break;
       if (!end) {
         const uint32_t dst0 = stbase + s * kStageBytes;
-        for (int c = ptid; c < kTileKeys * 72; c += kProdThreads) {
+        for (int c = ctid; c < kTileKeys * 72; c += kCopyThreads) {
           const int key = c / 72, ch = c % 72;
-          const int r = rows_s[s * 32 + key];
+          const int r = ring_rows[slot * 32 + key];
           const uint16_t* src = r >= 0 ? prm.kv + (size_t)r * prm.row_stride + ch * 8 : prm.kv;
           cp_async16(dst0 + (ch >> 3) * 4096 + sw128_offset(key, ch & 7), src, r >= 0 ? 16u : 0u);
         }
-        cp_async_commit();
-        // Publish this tile as soon as its own copies landed: the MMA warp
-        // looks one tile ahead before it runs PV on the current one, so a
-        // tile must never wait for the stage that PV frees.
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
+        cp_async_mbar_arrive_noinc(full + s);
+      } else {
         mbar_arrive(full + s);
-        ++i;
-        continue;
       }
-      mbar_arrive(full + s);  // end marker
-      break;
+      if (ctid == 0) {
+        st_mask[s] = mask;
+        st_end[s] = end ? 1u : 0u;
+        mbar_arrive(full + s);
+      }
+      mbar_arrive(rempty + slot);
+      if (end) break;
     }
     cp_async_wait<0>();
   } else {
@@ -370,17 +420,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const AttendPar
     int n = 0;
     bool ok = true;
     for (int i = 0;; ++i) {
-      const int s = i & 1;
-      if (!(ok = mbar_wait(full + s, (i >> 1) & 1, abort_flag))) break;
-      if (info_end[s]) break;
-      const uint32_t mask = info_mask[s];
-      if (!(ok = mbar_wait(sfull + s, (i >> 1) & 1, abort_flag))) break;
+      const int s = i % kStages;
+      if (!(ok = mbar_wait(full + s, (i / kStages) & 1, abort_flag))) break;
+      if (st_end[s]) break;
+      const uint32_t mask = st_mask[s];
+      if (!(ok = mbar_wait(sfull, i & 1, abort_flag))) break;
       tc_fence_after();
       uint32_t sv[32];
-      tmem_ld32(tmem + lane_base + s * kTileKeys, sv);
+      tmem_ld32(tmem + lane_base + kColS, sv);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(sempty + s);
+      mbar_arrive(sempty);
       float x[32];
       float mt = -INFINITY;
 #pragma unroll
@@ -436,6 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const AttendPar
     const bool hv = h < prm.H;
     const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
     const size_t orow = ((size_t)t * prm.H + h) * kDv + half * kDvHalf;
+    const float lse_v = l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
     if (prm.nsplit == 1) {
       for (int c = 0; c < kDvHalf / 32; ++c) {
         uint32_t ov[32];
@@ -459,8 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const AttendPar
           for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
-      if (hv && half == 0 && prm.lse)
-        prm.lse[(size_t)t * prm.H + h] = l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+      if (hv && half == 0 && prm.lse) prm.lse[(size_t)t * prm.H + h] = lse_v;
     } else {
       float* op = prm.o_part + ((size_t)split * prm.T * prm.H) * kDv;
       for (int c = 0; c < kDvHalf / 32; ++c) {
@@ -480,9 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const AttendPar
                                  __uint_as_float(ov[4 * v + 2]) * inv_l, __uint_as_float(ov[4 * v + 3]) * inv_l);
         }
       }
-      if (hv && half == 0)
-        prm.lse_part[((size_t)split * prm.T + t) * prm.H + h] =
-            l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+      if (hv && half == 0) prm.lse_part[((size_t)split * prm.T + t) * prm.H + h] = lse_v;
     }
   }
   tc_fence_before();
