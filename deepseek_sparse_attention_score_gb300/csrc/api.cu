@@ -1,5 +1,7 @@
 // extern "C" entry points of include/dsa.h: host-side argument checks,
 // workspace carving, and the kernel launches of each operation.
+#include <cudaTypedefs.h>
+
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -24,6 +26,47 @@ int sm_count() {
     cached[dev] = n;
   }
   return cached[dev];
+}
+
+void set_smem_attr_once(const void* func, int bytes) {
+  struct Entry {
+    const void* f;
+    int dev;
+  };
+  static Entry done[64];
+  static int ndone = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  for (int i = 0; i < ndone; ++i)
+    if (done[i].f == func && done[i].dev == dev) return;
+  cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (ndone < 64) done[ndone++] = {func, dev};
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_elems, uint32_t box_rows,
+                    uint64_t used_cols) {
+  auto fn = get_encode();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {used_cols, rows};
+  cuuint64_t strides[1] = {row_elems * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -26,8 +26,10 @@
 namespace dsa {
 
 namespace {
-constexpr int kThreads = 256;  // warp 0 MMA, warp 1 key generator, warps 2-3 gather, warps 4-7 softmax
-constexpr int kCopyThreads = 64;
+// warp 0 MMA, warp 1 key generator, warps 2-3 and 8-11 gather, warps 4-7 softmax
+constexpr int kThreads = 384;
+constexpr int kCopyWarps = 6;
+constexpr int kCopyThreads = kCopyWarps * 32;
 constexpr int kTileKeys = 32;
 constexpr int kStages = 5;   // KV tiles resident in shared memory
 constexpr int kRing = 8;     // key-address tiles generated (and L2-prefetched) ahead of the gather
@@ -42,7 +44,8 @@ constexpr int OFF_ST = OFF_QS + kQsBytes;
 constexpr int OFF_P = OFF_ST + kStages * kStageBytes;
 constexpr int OFF_RING = OFF_P + kPBytes;         // int32 [kRing][32] physical rows
 constexpr int OFF_RINFO = OFF_RING + kRing * 32 * 4;  // uint32 mask[kRing], end[kRing]
-constexpr int OFF_SINFO = OFF_RINFO + kRing * 8;      // uint32 mask[kStages], end[kStages]
+constexpr int OFF_RBASE = OFF_RINFO + kRing * 8;      // int32 base row of contiguous tiles [kRing]
+constexpr int OFF_SINFO = OFF_RBASE + kRing * 4;      // uint32 mask[kStages], end[kStages]
 constexpr int OFF_BAR = (OFF_SINFO + kStages * 8 + 7) & ~7;
 constexpr int NBAR = 2 * kStages + 2 * kRing + 5;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -54,36 +57,46 @@ constexpr uint32_t kColQ = 0;    // 224 columns of packed bf16 pairs
 constexpr uint32_t kColS = 224;  // 32 fp32 columns
 constexpr uint32_t kColO = 256;  // 256 fp32 columns
 constexpr float kRescaleThreshold = 8.f;  // log2 units: p stays <= 256
+constexpr int kMaxSplits = 8;
 }  // namespace
 
 // Warp-wide generator of 32-key tiles. Every lane gets the flat physical row
 // of "its" key (or -1) and the ballot of valid keys; returns false when the
-// CTA's key list is exhausted. Runs on one full warp.
+// CTA's key list is exhausted. Runs on one full warp. Loads are batched so a
+// whole window of selections (8 x 32 token entries, or 32 pages / union
+// slots) resolves to physical rows in two or three dependent global loads.
 struct TileGen {
+  static constexpr int GB = 8;  // token windows resolved per refill
   const AttendParams* p;
   int mode, t, seq, pos, kv_len, n_vis, page_base;
-  // token / page modes
-  int e, e1, sub;
-  uint32_t pend;      // page mode: entries of the current 32-window still to visit
-  int win;            // page / qblock: start of the current 32-window
-  int cur, cur_valid; // current page entry (page mode) or unit (qblock)
-  // qblock
-  int b, qq, cnt;
+  int e, e1;          // token / page modes: next entry, end of this CTA's range
+  int win;            // page / qblock: start of the next 32-window
+  // token mode: buffered tiles
+  int buf_row[GB];
+  uint32_t buf_mask[GB];
+  int buf_n, buf_i;
+  // page / qblock modes: current window
+  uint32_t pend;      // units of the window still to visit
+  int w_key0;         // this lane's unit: first key position (page) or kp base (qblock)
+  int w_phys;         // this lane's unit: physical page, -1 if none
+  int cur_key0, cur_phys, sub, cur_valid;
+  int b, qq, cnt;     // qblock
 
   __device__ void init(const AttendParams& prm, int tok, int split) {
     p = &prm;
     mode = prm.mode;
     t = tok;
+    const int sq = seq_of_token_warp(prm.cu_q_lens, prm.S, tok);
     TokenGeom g = token_geom(prm.seq_lens, prm.cu_q_lens, prm.cu_kv_lens, prm.S, prm.ps, 0x3fffffff, tok,
-                             prm.dev_status);
+                             prm.dev_status, sq);
     seq = g.seq;
     pos = g.pos;
     kv_len = g.kv_len;
     n_vis = g.n_vis;
     page_base = g.page_base;
-    sub = 0;
+    buf_n = buf_i = 0;
     pend = 0;
-    cur = -1;
+    sub = 0;
     cur_valid = 0;
     if (mode == kModeQblock) {
       b = tok / prm.QB;
@@ -98,10 +111,9 @@ struct TileGen {
     }
   }
 
-  // physical flat row of sequence-local key position j (page entry checked)
-  __device__ __forceinline__ long long phys_row(int j) const {
-    const int ent = page_base + j / p->ps;
-    if (ent >= p->PTW) {
+  // physical page of packed page-table entry `ent` (checked), or -1
+  __device__ __forceinline__ int page_of(int ent) const {
+    if (ent < 0 || ent >= p->PTW) {
       set_status(p->dev_status, DSA_STATUS_BAD_INDEX);
       return -1;
     }
@@ -110,97 +122,111 @@ struct TileGen {
       set_status(p->dev_status, DSA_STATUS_BAD_METADATA);
       return -1;
     }
-    return (long long)pg * p->ps + j % p->ps;
+    return pg;
   }
 
-  __device__ bool next(long long& row, uint32_t& mask) {
+  // base: first physical row of the tile when its 32 keys are 32 consecutive
+  // rows of one page (page and qblock modes), else -1
+  __device__ bool next(long long& row, uint32_t& mask, long long& base) {
     const int lane = lane_id();
-    const int tiles_per_unit = p->ps / kTileKeys;
-    while (true) {
-      if (mode == kModeToken) {
+    const int ps = p->ps;
+    base = -1;
+    if (mode == kModeToken) {
+      while (buf_i == buf_n) {
         if (e >= e1) return false;
-        const int ee = e + lane;
-        const int j = ee < e1 ? __ldg(p->sel + (size_t)t * p->K + ee) : -1;
-        const bool v = j >= 0 && j < n_vis;
-        row = v ? phys_row(j) : -1;
-        mask = __ballot_sync(0xffffffffu, v && row >= 0);
-        e += 32;
-        if (mask) return true;
-        continue;
+        int j[GB];
+#pragma unroll
+        for (int g = 0; g < GB; ++g) {
+          const int ee = e + 32 * g + lane;
+          j[g] = ee < e1 ? __ldg(p->sel + (size_t)t * p->K + ee) : -1;
+        }
+        int pg[GB];
+#pragma unroll
+        for (int g = 0; g < GB; ++g) pg[g] = (j[g] >= 0 && j[g] < n_vis) ? page_of(page_base + j[g] / ps) : -1;
+        buf_n = buf_i = 0;
+#pragma unroll
+        for (int g = 0; g < GB; ++g) {
+          const bool v = pg[g] >= 0;
+          const uint32_t m = __ballot_sync(0xffffffffu, v);
+          if (m) {
+            buf_row[buf_n] = v ? pg[g] * ps + j[g] % ps : -1;
+            buf_mask[buf_n] = m;
+            ++buf_n;
+          }
+        }
+        e += 32 * GB;
       }
-      // page and qblock modes walk units of ps keys, 32 keys per tile
+      // registers are indexed dynamically here; GB is small
+      int r = -1;
+      uint32_t m = 0;
+#pragma unroll
+      for (int g = 0; g < GB; ++g)
+        if (g == buf_i) {
+          r = buf_row[g];
+          m = buf_mask[g];
+        }
+      ++buf_i;
+      row = r;
+      mask = m;
+      return true;
+    }
+    const int tiles_per_unit = ps / kTileKeys;
+    while (true) {
       if (cur_valid && sub < tiles_per_unit) {
         const int k0 = sub * kTileKeys + lane;
         bool v;
-        long long r = -1;
         if (mode == kModePage) {
-          const int j = cur * p->ps + k0;
-          v = j < n_vis;
-          if (v) r = phys_row(j);
+          v = cur_key0 + k0 < n_vis;
         } else {
-          // qblock: unit g = cur, kp = g*ps + r - base_tok
-          const long long kp = (long long)cur * p->ps + k0 - (long long)page_base * p->ps;
+          const int kp = cur_key0 + k0;  // kp = g*ps + r - base_tok
           v = kp <= pos && kp < kv_len;
-          if (v) {
-            const int pg = __ldg(p->page_indices + cur);
-            if (pg < 0 || pg >= p->P) {
-              set_status(p->dev_status, DSA_STATUS_BAD_METADATA);
-              v = false;
-            } else {
-              r = (long long)pg * p->ps + k0;
-            }
-          }
         }
+        base = (long long)cur_phys * ps + sub * kTileKeys;
         ++sub;
-        row = v ? r : -1;
-        mask = __ballot_sync(0xffffffffu, v && r >= 0);
+        row = v ? (long long)cur_phys * ps + k0 : -1;
+        mask = __ballot_sync(0xffffffffu, v);
         if (mask) return true;
         continue;
       }
-      // advance to the next unit
       cur_valid = 0;
       sub = 0;
       if (!pend) {
-        // refill a window of 32 candidate units
+        // resolve a window of 32 candidate units to physical pages
         if (mode == kModePage) {
           if (win >= e1) return false;
           const int ee = win + lane;
-          const int pg = ee < e1 ? __ldg(p->sel + (size_t)t * p->K + ee) : -1;
-          pend = __ballot_sync(0xffffffffu, pg >= 0 && (long long)pg * p->ps < n_vis);
+          const int pgl = ee < e1 ? __ldg(p->sel + (size_t)t * p->K + ee) : -1;
+          const bool v = pgl >= 0 && (long long)pgl * ps < n_vis;
+          w_phys = v ? page_of(page_base + pgl) : -1;
+          w_key0 = pgl * ps;
         } else {
           if (win >= cnt) return false;
           const int u = win + lane;
           bool has = false;
+          int g = -1;
           if (u < cnt) {
-            const uint32_t wd =
-                __ldg(p->member + ((size_t)b * p->u_max + u) * (p->QB / 32) + (qq >> 5));
+            const uint32_t wd = __ldg(p->member + ((size_t)b * p->u_max + u) * (p->QB / 32) + (qq >> 5));
+            g = __ldg(p->units + (size_t)b * p->u_max + u);
             has = (wd >> (qq & 31)) & 1u;
           }
-          pend = __ballot_sync(0xffffffffu, has);
+          w_phys = has ? page_of(g) : -1;
+          w_key0 = (g - page_base) * ps;
         }
+        pend = __ballot_sync(0xffffffffu, w_phys >= 0);
         win += 32;
         continue;
       }
       const int bit = __ffs(pend) - 1;
       pend &= pend - 1u;
-      const int idx = win - 32 + bit;
-      if (mode == kModePage) {
-        cur = __ldg(p->sel + (size_t)t * p->K + idx);
-        cur_valid = 1;
-      } else {
-        const int g = __ldg(p->units + (size_t)b * p->u_max + idx);
-        if (g < 0 || g >= p->PTW) {
-          if (lane == 0) set_status(p->dev_status, DSA_STATUS_BAD_INDEX);
-          continue;
-        }
-        cur = g;
-        cur_valid = 1;
-      }
+      cur_phys = __shfl_sync(0xffffffffu, w_phys, bit);
+      cur_key0 = __shfl_sync(0xffffffffu, w_key0, bit);
+      cur_valid = 1;
     }
   }
 };
 
-__global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const AttendParams prm) {
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_mla_kernel(const AttendParams prm, const __grid_constant__ CUtensorMap kvmap) {
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {
     if (threadIdx.x == 0) set_status(prm.dev_status, DSA_STATUS_INTERNAL);
@@ -216,6 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const AttendPar
   int* ring_rows = reinterpret_cast<int*>(smem + OFF_RING);
   volatile uint32_t* ring_mask = reinterpret_cast<volatile uint32_t*>(smem + OFF_RINFO);
   volatile uint32_t* ring_end = ring_mask + kRing;
+  volatile int* ring_base = reinterpret_cast<volatile int*>(smem + OFF_RBASE);
   volatile uint32_t* st_mask = reinterpret_cast<volatile uint32_t*>(smem + OFF_SINFO);
   volatile uint32_t* st_end = st_mask + kStages;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -254,33 +281,50 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const AttendPar
   }
   const int nh = min(128, prm.H - h0);
   const uint16_t* qt = prm.q + ((size_t)t * prm.H + h0) * kDk;
-  // Q[:, 448:576] -> two 128-byte-swizzled column blocks in shared memory
-  {
-    const uint32_t qbase = smem_u32(qs_s);
-    constexpr int CH = (kDk - kQTmemDims) / 8;  // 16 chunks of 16 bytes per row
-    for (int c = tid; c < 128 * CH; c += kThreads) {
+  // Q[:, 448:576] -> two 128-byte-swizzled column blocks in shared memory;
+  // Q[:, 0:448] staged row-major (912-byte rows, conflict-free 16-byte reads)
+  // in the still unused KV ring, then moved into TMEM by the softmax warps.
+  constexpr int kQRowStage = kQTmemDims * 2 + 16;
+  // The key generator (warp 1) resolves its first window of selections while
+  // the other warps stage Q; it publishes tiles only after the barrier below.
+  TileGen gen;
+  bool gen_more = false;
+  long long gen_row = -1, gen_base = -1;
+  uint32_t gen_mask = 0;
+  if (warp == 1) {
+    gen.init(prm, t, split);
+    gen_more = gen.next(gen_row, gen_mask, gen_base);
+  } else {
+    const uint32_t qbase = smem_u32(qs_s), stage = smem_u32(st_s);
+    constexpr int CH = kDk / 8;  // 72 chunks of 16 bytes per row
+    const int qtid = tid < 32 ? tid : tid - 32;  // warp 1 is busy generating keys
+    for (int c = qtid; c < 128 * CH; c += kThreads - 32) {
       const int r = c / CH, ch = c % CH;
       const bool ok = r < nh;
-      const uint16_t* src = ok ? qt + (size_t)r * kDk + kQTmemDims + ch * 8 : prm.q;
-      cp_async16(qbase + (ch >> 3) * 16384 + sw128_offset(r, ch & 7), src, ok ? 16u : 0u);
+      const uint16_t* src = ok ? qt + (size_t)r * kDk + ch * 8 : prm.q;
+      const uint32_t dst = ch < kQTmemDims / 8
+                               ? stage + r * kQRowStage + ch * 16
+                               : qbase + ((ch - kQTmemDims / 8) >> 3) * 16384 + sw128_offset(r, ch & 7);
+      cp_async16(dst, src, ok ? 16u : 0u);
     }
     cp_async_commit();
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (warp >= 4) {
-    // Q[:, 0:448] -> TMEM lanes (one head row per lane), bf16 pairs per column
+  if (warp >= 4 && warp < 8) {
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint4* src = reinterpret_cast<const uint4*>(qt + (size_t)r * kDk);
+    const uint4* src = reinterpret_cast<const uint4*>(st_s + r * kQRowStage);
 #pragma unroll 1
     for (int c0 = 0; c0 < kQTmemDims / 2; c0 += 32) {
       uint32_t v[32];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const uint4 x = r < nh ? __ldg(src + c0 / 4 + j) : make_uint4(0, 0, 0, 0);
+        const uint4 x = src[c0 / 4 + j];
         v[4 * j] = x.x;
         v[4 * j + 1] = x.y;
         v[4 * j + 2] = x.z;
@@ -290,8 +334,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const AttendPar
     }
     tmem_st_wait();
   }
-  cp_async_wait<0>();
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -358,31 +400,30 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const AttendPar
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ key generator + L2 prefetch
-    TileGen gen;
-    gen.init(prm, t, split);
+    // ------------------------------------------------------------ key generator
     for (int j = 0;; ++j) {
-      long long row = -1;
-      uint32_t mask = 0;
-      const bool more = gen.next(row, mask);
+      long long row = gen_row, base = gen_base;
+      uint32_t mask = gen_mask;
+      const bool more = j == 0 ? gen_more : gen.next(row, mask, base);
       const int slot = j % kRing;
       int ok = 1;
       if (lane == 0) ok = mbar_wait(rempty + slot, ((j / kRing) & 1) ^ 1, abort_flag) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       ring_rows[slot * 32 + lane] = more ? (int)row : -1;
-      if (more && row >= 0) prefetch_l2_bulk(prm.kv + (size_t)row * prm.row_stride, kDk * 2);
       if (lane == 0) {
         ring_mask[slot] = mask;
         ring_end[slot] = more ? 0u : 1u;
+        ring_base[slot] = more ? (int)base : -1;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(rfull + slot);
       if (!more) break;
     }
-  } else if (warp < 4) {
+  } else if (warp < 4 || warp >= 8) {
     // ------------------------------------------------------------ gather
-    const int ctid = tid - 64;
+    const int cw = warp < 4 ? warp - 2 : warp - 6;  // 0..5
+    const int ctid = cw * 32 + lane;
     const uint32_t stbase = smem_u32(st_s);
     for (int i = 0;; ++i) {
       const int slot = i % kRing, s = i % kStages;
@@ -390,13 +431,31 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const AttendPar
       const bool end = ring_end[slot] != 0;
       const uint32_t mask = ring_mask[slot];
       if (!mbar_wait(empty + s, ((i / kStages) & 1) ^ 1, abort_flag)) break;
-      if (!end) {
+      const int cbase = ring_base[slot];
+      if (!end && cbase >= 0) {
+        // 32 consecutive rows of one page: nine 2-D TMA boxes (64 cols x 32 rows)
+        if (ctid == 0) {
+          uint8_t* dst = st_s + s * kStageBytes;
+          mbar_arrive_expect_tx(full + s, kStageBytes);
+#pragma unroll 1
+          for (int c = 0; c < kDk / 64; ++c) tma_load_2d(dst + c * 4096, &kvmap, full + s, c * 64, cbase);
+        } else {
+          mbar_arrive(full + s);
+        }
+      } else if (!end) {
+        // scattered rows: copier warp cw copies keys cw, cw+6, ...; per key three
+        // coalesced 512-byte instructions (chunks lane, lane+32, lane+64 of 72)
         const uint32_t dst0 = stbase + s * kStageBytes;
-        for (int c = ctid; c < kTileKeys * 72; c += kCopyThreads) {
-          const int key = c / 72, ch = c % 72;
+#pragma unroll 2
+        for (int key = cw; key < kTileKeys; key += kCopyWarps) {
           const int r = ring_rows[slot * 32 + key];
-          const uint16_t* src = r >= 0 ? prm.kv + (size_t)r * prm.row_stride + ch * 8 : prm.kv;
-          cp_async16(dst0 + (ch >> 3) * 4096 + sw128_offset(key, ch & 7), src, r >= 0 ? 16u : 0u);
+          const uint16_t* rb = r >= 0 ? prm.kv + (size_t)r * prm.row_stride : prm.kv;
+          const uint32_t nb = r >= 0 ? 16u : 0u;
+#pragma unroll
+          for (int part = 0; part < 3; ++part) {
+            const int ch = lane + 32 * part;
+            if (ch < 72) cp_async16(dst0 + (ch >> 3) * 4096 + sw128_offset(key, ch & 7), rb + ch * 8, nb);
+          }
         }
         cp_async_mbar_arrive_noinc(full + s);
       } else {
@@ -512,6 +571,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const AttendPar
       }
       if (hv && half == 0 && prm.lse) prm.lse[(size_t)t * prm.H + h] = lse_v;
     } else {
+      // split keys: write this split's normalised partial; the last CTA of the
+      // (token, value half) group merges all splits and writes the output.
       float* op = prm.o_part + ((size_t)split * prm.T * prm.H) * kDv;
       for (int c = 0; c < kDvHalf / 32; ++c) {
         uint32_t ov[32];
@@ -530,7 +591,71 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const AttendPar
                                  __uint_as_float(ov[4 * v + 2]) * inv_l, __uint_as_float(ov[4 * v + 3]) * inv_l);
         }
       }
-      if (hv && half == 0) prm.lse_part[((size_t)split * prm.T + t) * prm.H + h] = lse_v;
+      // lse of this split as seen by this CTA (both value halves compute the
+      // same logits, so each group merges with its own copies)
+      float* lsep = prm.lse_part + (size_t)gridDim.x * 128;
+      lsep[(((size_t)split * prm.T + t) * gridDim.x + blockIdx.x) * 128 + r] = lse_v;
+      __threadfence();
+      named_bar_sync(2, 128);
+      volatile int* s_last = abort_flag + 1;
+      if (r == 0) {
+        int* ctr = prm.counters + (size_t)t * gridDim.x + blockIdx.x;
+        const int old = atomicAdd(ctr, 1);
+        const int last = old == prm.nsplit - 1;
+        if (last) *ctr = 0;  // ready for the next call
+        *s_last = last;
+      }
+      named_bar_sync(2, 128);
+      if (*s_last && hv) {
+        __threadfence();
+        float wz[kMaxSplits];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int z = 0; z < kMaxSplits; ++z) {
+          if (z >= prm.nsplit) break;
+          wz[z] = __ldcg(prm.lse_part + (size_t)gridDim.x * 128 +
+                         (((size_t)z * prm.T + t) * gridDim.x + blockIdx.x) * 128 + r);
+          mx = fmaxf(mx, wz[z]);
+        }
+        float tot = 0.f;
+        for (int z = 0; z < prm.nsplit; ++z) {
+          wz[z] = (mx == -INFINITY || wz[z] == -INFINITY) ? 0.f : exp2f((wz[z] - mx) * 1.4426950408889634f);
+          tot += wz[z];
+        }
+        const float inv = tot > 0.f ? 1.f / tot : 0.f;
+        for (int c = 0; c < kDvHalf; c += 8) {
+          float4 v0[kMaxSplits], v1[kMaxSplits];
+#pragma unroll
+          for (int z = 0; z < kMaxSplits; ++z) {
+            if (z < prm.nsplit) {
+              const float* src = prm.o_part + ((size_t)z * prm.T * prm.H) * kDv + orow + c;
+              v0[z] = __ldcg(reinterpret_cast<const float4*>(src));
+              v1[z] = __ldcg(reinterpret_cast<const float4*>(src + 4));
+            }
+          }
+          float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int z = 0; z < kMaxSplits; ++z) {
+            if (z < prm.nsplit) {
+              const float wgt = wz[z] * inv;
+              a[0] = fmaf(wgt, v0[z].x, a[0]);
+              a[1] = fmaf(wgt, v0[z].y, a[1]);
+              a[2] = fmaf(wgt, v0[z].z, a[2]);
+              a[3] = fmaf(wgt, v0[z].w, a[3]);
+              a[4] = fmaf(wgt, v1[z].x, a[4]);
+              a[5] = fmaf(wgt, v1[z].y, a[5]);
+              a[6] = fmaf(wgt, v1[z].z, a[6]);
+              a[7] = fmaf(wgt, v1[z].w, a[7]);
+            }
+          }
+          __nv_bfloat162 b0 = __floats2bfloat162_rn(a[0], a[1]), b1 = __floats2bfloat162_rn(a[2], a[3]);
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(a[4], a[5]), b3 = __floats2bfloat162_rn(a[6], a[7]);
+          *reinterpret_cast<uint4*>(prm.o + orow + c) =
+              make_uint4(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1),
+                         *reinterpret_cast<uint32_t*>(&b2), *reinterpret_cast<uint32_t*>(&b3));
+        }
+        if (half == 0 && prm.lse) prm.lse[(size_t)t * prm.H + h] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+      }
     }
   }
   tc_fence_before();
@@ -542,72 +667,50 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const AttendPar
   }
 }
 
-// Merge split-key partials: o = sum_z e^{lse_z - M} o_z / sum_z e^{lse_z - M}.
-__global__ void __launch_bounds__(256) combine_splits_kernel(const float* __restrict__ o_part,
-                                                             const float* __restrict__ lse_part, int nsplit, int T,
-                                                             int H, uint16_t* __restrict__ o, float* __restrict__ lse) {
-  const int th = blockIdx.x;  // (t, h)
-  if (th >= T * H) return;
-  __shared__ float wts[16];
-  __shared__ float s_lse;
-  if (threadIdx.x == 0) {
-    float mx = -INFINITY;
-    for (int z = 0; z < nsplit; ++z) mx = fmaxf(mx, lse_part[(size_t)z * T * H + th]);
-    float tot = 0.f;
-    for (int z = 0; z < nsplit; ++z) {
-      const float l = lse_part[(size_t)z * T * H + th];
-      const float wz = (mx == -INFINITY || l == -INFINITY) ? 0.f : __expf(l - mx);
-      wts[z] = wz;
-      tot += wz;
-    }
-    for (int z = 0; z < nsplit; ++z) wts[z] = tot > 0.f ? wts[z] / tot : 0.f;
-    s_lse = tot > 0.f ? mx + __logf(tot) : -INFINITY;
-  }
-  __syncthreads();
-  const int c = threadIdx.x * 2;  // 256 threads x 2 columns = 512
-  float a0 = 0.f, a1 = 0.f;
-  for (int z = 0; z < nsplit; ++z) {
-    const float2 v = *reinterpret_cast<const float2*>(o_part + ((size_t)z * T * H + th) * kDv + c);
-    a0 = fmaf(wts[z], v.x, a0);
-    a1 = fmaf(wts[z], v.y, a1);
-  }
-  __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
-  *reinterpret_cast<__nv_bfloat162*>(o + (size_t)th * kDv + c) = b2;
-  if (lse && threadIdx.x == 0) lse[th] = s_lse;
-}
-
+// Split the key list only as far as one wave of CTAs (one per SM) allows:
+// more splits cost partial-output traffic and leave a quantised tail.
 int attend_num_splits(int T, int H, int K, int mode) {
   if (mode == kModeQblock) return 1;
   const int ctas = T * 2 * ((H + 127) / 128);
-  const int target = 2 * sm_count();
-  int z = ctas >= target ? 1 : (target + ctas - 1) / ctas;
+  int z = max(1, sm_count() / max(1, ctas));
   const int max_by_k = mode == kModeToken ? max(1, (K + 31) / 32) : max(1, K);
-  z = min(z, min(16, max_by_k));
+  z = min(z, min(kMaxSplits, max_by_k));
   return max(1, z);
 }
 
+// Split-key workspace: fp32 partial outputs [nsplit, T, H, 512], per-CTA lse
+// copies [nsplit, T, CTAs per token, 128] (offset by one CTA row of padding),
+// and one arrival counter per (token, CTA column).
+static size_t part_bytes(int T, int H, int nsplit) { return align_up((size_t)nsplit * T * H * kDv * 4, 256); }
+static size_t lse_bytes(int T, int H, int nsplit) {
+  const size_t cols = 2 * (size_t)((H + 127) / 128);
+  return align_up(((size_t)nsplit * T * cols + cols) * 128 * 4, 256);
+}
 size_t attend_workspace_bytes(int T, int H, int nsplit) {
   if (nsplit <= 1) return 0;
-  return align_up((size_t)nsplit * T * H * kDv * 4, 256) + align_up((size_t)nsplit * T * H * 4, 256);
+  const size_t cols = 2 * (size_t)((H + 127) / 128);
+  return part_bytes(T, H, nsplit) + lse_bytes(T, H, nsplit) + align_up((size_t)T * cols * 4, 256);
 }
 
 int run_attend(cudaStream_t stream, AttendParams prm, void* ws, size_t ws_bytes) {
   if (prm.T == 0 || prm.H == 0) return DSA_OK;
+  const int cols = 2 * ((prm.H + 127) / 128);
   if (prm.nsplit > 1) {
     if (!ws || ws_bytes < attend_workspace_bytes(prm.T, prm.H, prm.nsplit)) return DSA_ERR_WORKSPACE;
-    prm.o_part = static_cast<float*>(ws);
-    prm.lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
-                                            align_up((size_t)prm.nsplit * prm.T * prm.H * kDv * 4, 256));
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    prm.o_part = reinterpret_cast<float*>(base);
+    prm.lse_part = reinterpret_cast<float*>(base + part_bytes(prm.T, prm.H, prm.nsplit));
+    prm.counters = reinterpret_cast<int*>(base + part_bytes(prm.T, prm.H, prm.nsplit) +
+                                          lse_bytes(prm.T, prm.H, prm.nsplit));
+    if (cudaMemsetAsync(prm.counters, 0, (size_t)prm.T * cols * 4, stream) != cudaSuccess) return DSA_ERR_CUDA;
   }
-  cudaFuncSetAttribute(sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-  dim3 grid(2 * ((prm.H + 127) / 128), prm.T, prm.nsplit);
-  sparse_mla_kernel<<<grid, kThreads, kSmem, stream>>>(prm);
+  CUtensorMap kvmap;
+  if (!encode_bf16_2d(&kvmap, prm.kv, (uint64_t)prm.P * prm.ps, (uint64_t)prm.row_stride, 32, kDk))
+    return DSA_ERR_CUDA;
+  set_smem_attr_once(reinterpret_cast<const void*>(sparse_mla_kernel), kSmem);
+  dim3 grid(cols, prm.T, prm.nsplit);
+  sparse_mla_kernel<<<grid, kThreads, kSmem, stream>>>(prm, kvmap);
   DSA_CHECK_LAUNCH();
-  if (prm.nsplit > 1) {
-    combine_splits_kernel<<<prm.T * prm.H, 256, 0, stream>>>(prm.o_part, prm.lse_part, prm.nsplit, prm.T, prm.H,
-                                                            prm.o, prm.lse);
-    DSA_CHECK_LAUNCH();
-  }
   return DSA_OK;
 }
 

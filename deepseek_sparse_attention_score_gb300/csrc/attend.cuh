@@ -29,7 +29,8 @@ struct AttendParams {
   uint16_t* o;      // bf16 [T, H, 512]
   float* lse;       // [T, H] or null
   float* o_part;    // [nsplit, T, H, 512] (set by run_attend)
-  float* lse_part;  // [nsplit, T, H]
+  float* lse_part;  // per-CTA lse copies (set by run_attend)
+  int* counters;    // split arrival counters (set by run_attend)
   int32_t* dev_status;
 };
 

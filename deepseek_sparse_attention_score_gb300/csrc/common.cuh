@@ -25,6 +25,24 @@ __device__ __forceinline__ int seq_of_token(const int32_t* cu_q_lens, int S, int
   return lo;
 }
 
+// Warp-cooperative version of seq_of_token: 32 boundaries per step, so a
+// batch of S requests resolves in ceil(log32(S)) dependent loads. All lanes
+// must call it with the same t; every lane gets the result.
+__device__ __forceinline__ int seq_of_token_warp(const int32_t* cu_q_lens, int S, int t) {
+  const int lane = threadIdx.x & 31;
+  int lo = 0, hi = S;  // answer in [lo, hi)
+  while (hi - lo > 1) {
+    const int step = (hi - lo + 31) / 32;
+    const int idx = lo + lane * step;
+    const bool le = idx < hi && __ldg(cu_q_lens + idx) <= t;
+    const uint32_t m = __ballot_sync(0xffffffffu, le);
+    const int last = 31 - __clz(m);  // lane 0 always qualifies (cu_q_lens[lo] <= t)
+    lo = lo + last * step;
+    hi = min(hi, lo + step);
+  }
+  return lo;
+}
+
 // Per-token geometry derived from the ragged metadata.
 struct TokenGeom {
   int seq;       // request id
@@ -36,9 +54,9 @@ struct TokenGeom {
 
 __device__ __forceinline__ TokenGeom token_geom(const int32_t* seq_lens, const int32_t* cu_q_lens,
                                                 const int32_t* cu_kv_lens, int S, int ps, int max_kv, int t,
-                                                int32_t* dev_status) {
+                                                int32_t* dev_status, int seq = -1) {
   TokenGeom g;
-  g.seq = seq_of_token(cu_q_lens, S, t);
+  g.seq = seq >= 0 ? seq : seq_of_token(cu_q_lens, S, t);
   const int q0 = __ldg(cu_q_lens + g.seq), q1 = __ldg(cu_q_lens + g.seq + 1);
   int kv = __ldg(seq_lens + g.seq);
   if (kv < 0 || kv > max_kv || kv < q1 - q0) {
@@ -71,5 +89,13 @@ void note_launch();  // process-wide count of enqueued kernels
 
 namespace dsa {
 int sm_count();  // cached per device
+// Raise a kernel's dynamic shared-memory limit once per device (not during
+// stream capture after the first call).
+void set_smem_attr_once(const void* func, int bytes);
+// 2-D bf16 tensor map over a row-major matrix of `rows` rows whose rows are
+// `row_elems` elements apart, exposing the first `used_cols` columns, with a
+// [64 cols x box_rows] box and 128-byte swizzle.
+bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_elems, uint32_t box_rows,
+                    uint64_t used_cols);
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 }  // namespace dsa

@@ -12,8 +12,6 @@
 // A device-side planner turns the ragged metadata into work items
 // (query tile, key chunk) so the persistent kernels never read metadata the
 // host cannot see.
-#include <cudaTypedefs.h>
-
 #include "common.cuh"
 #include "indexer.cuh"
 
@@ -210,50 +208,80 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::THREADS, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
+    // The whole warp walks the items so that an item's page ids are resolved
+    // with one batch of loads (up to 64 pages, two per lane); lane 0 issues
+    // the TMA copies.
     if (lane == 0) {
       prefetch_tmap(&kmap);
       prefetch_tmap(&qmap);
-      int kt = 0, it = 0;
-      bool ok = true;
-      for (int ii = blockIdx.x; ii < n_items && ok; ii += gridDim.x, ++it) {
-        const int4 item = items[ii];
-        const int t0 = item.x, ntok = item.y >> 24, seq = item.y & 0xFFFFFF, kb = item.z, ke = item.w;
-        const int qb = it & 1;
-        if (!(ok = mbar_wait(qempty + qb, ((it >> 1) & 1) ^ 1, abort_flag))) break;
-        mbar_arrive_expect_tx(qfull + qb, C::Q_BYTES + ntok * 128);
-        tma_load_2d(q_s + qb * C::Q_BYTES, &qmap, qfull + qb, 0, t0 * 32);
-        tma_load_2d(q_s + qb * C::Q_BYTES + C::N * 128, &qmap, qfull + qb, 64, t0 * 32);
-        bulk_load(w_s + qb * C::N, m.w + (size_t)t0 * 32, ntok * 128, qfull + qb);
-        const int page_base = __ldg(m.cu_kv_lens + seq) / m.ps;
-        const int ppt = 128 / m.ps;  // pages per 128-key tile
-        for (int tile = kb / 128; tile * 128 < ke && ok; ++tile, ++kt) {
-          const int s = kt % C::STAGES;
-          if (!(ok = mbar_wait(empty + s, ((kt / C::STAGES) & 1) ^ 1, abort_flag))) break;
-          int phys[4];
-          int nload = 0;
-          for (int pg = 0; pg < ppt; ++pg) {
-            const int key0 = tile * 128 + pg * m.ps;
-            phys[pg] = -1;
-            if (key0 < ke) {
-              const int p = __ldg(m.page_indices + page_base + key0 / m.ps);
-              if (p >= 0 && p < m.P) {
-                phys[pg] = p;
-                ++nload;
-              } else {
-                set_status(m.dev_status, DSA_STATUS_BAD_METADATA);
-              }
-            }
-          }
-          mbar_arrive_expect_tx(full + s, nload * m.ps * 256);
-          uint8_t* dst = st_s + s * C::STAGE_BYTES;
-          for (int pg = 0; pg < ppt; ++pg) {
-            if (phys[pg] < 0) continue;
-            tma_load_2d(dst + pg * m.ps * 128, &kmap, full + s, 0, phys[pg] * m.ps);
-            tma_load_2d(dst + 16384 + pg * m.ps * 128, &kmap, full + s, 64, phys[pg] * m.ps);
-          }
+    }
+    int kt = 0, it = 0;
+    bool ok = true;
+    for (int ii = blockIdx.x; ii < n_items && ok; ii += gridDim.x, ++it) {
+      const int4 item = items[ii];
+      const int t0 = item.x, ntok = item.y >> 24, seq = item.y & 0xFFFFFF, kb = item.z, ke = item.w;
+      const int qb = it & 1;
+      int okl = 1;
+      if (lane == 0) {
+        okl = mbar_wait(qempty + qb, ((it >> 1) & 1) ^ 1, abort_flag) ? 1 : 0;
+        if (okl) {
+          mbar_arrive_expect_tx(qfull + qb, C::Q_BYTES + ntok * 128);
+          tma_load_2d(q_s + qb * C::Q_BYTES, &qmap, qfull + qb, 0, t0 * 32);
+          tma_load_2d(q_s + qb * C::Q_BYTES + C::N * 128, &qmap, qfull + qb, 64, t0 * 32);
+          bulk_load(w_s + qb * C::N, m.w + (size_t)t0 * 32, ntok * 128, qfull + qb);
         }
       }
-      // drain: make sure no TMA write is still landing in shared memory
+      if (!(ok = __shfl_sync(0xffffffffu, okl, 0) != 0)) break;
+      const int ps = m.ps;
+      const int page_base = __ldg(m.cu_kv_lens + seq) / ps;
+      const int pg0 = kb / ps, npg = (ke - 1) / ps - pg0 + 1;  // <= 64 pages per item
+      int pid[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int pi = lane + 32 * h;
+        pid[h] = -1;
+        if (pi < npg) {
+          const int p = __ldg(m.page_indices + page_base + pg0 + pi);
+          if (p >= 0 && p < m.P) pid[h] = p;
+          else set_status(m.dev_status, DSA_STATUS_BAD_METADATA);
+        }
+      }
+      const int ppt = 128 / ps;  // pages per 128-key tile
+      for (int tile = kb / 128; tile * 128 < ke; ++tile, ++kt) {
+        const int s = kt % C::STAGES;
+        int phys[4];
+        int nload = 0;
+#pragma unroll
+        for (int pg = 0; pg < 4; ++pg) {
+          phys[pg] = -1;
+          const int key0 = tile * 128 + pg * ps;
+          if (pg < ppt) {
+            const int pi = key0 / ps - pg0;
+            const int v0 = __shfl_sync(0xffffffffu, pid[0], pi & 31);
+            const int v1 = __shfl_sync(0xffffffffu, pid[1], pi & 31);
+            if (key0 < ke) {
+              phys[pg] = pi < 32 ? v0 : v1;
+              if (phys[pg] >= 0) ++nload;
+            }
+          }
+        }
+        if (lane == 0) {
+          okl = mbar_wait(empty + s, ((kt / C::STAGES) & 1) ^ 1, abort_flag) ? 1 : 0;
+          if (okl) {
+            mbar_arrive_expect_tx(full + s, nload * ps * 256);
+            uint8_t* dst = st_s + s * C::STAGE_BYTES;
+            for (int pg = 0; pg < ppt; ++pg) {
+              if (phys[pg] < 0) continue;
+              tma_load_2d(dst + pg * ps * 128, &kmap, full + s, 0, phys[pg] * ps);
+              tma_load_2d(dst + 16384 + pg * ps * 128, &kmap, full + s, 64, phys[pg] * ps);
+            }
+          }
+        }
+        if (!(ok = __shfl_sync(0xffffffffu, okl, 0) != 0)) break;
+      }
+    }
+    // drain: make sure no TMA write is still landing in shared memory
+    if (lane == 0) {
       for (int d = 1; d <= C::STAGES && d <= kt; ++d) {
         const int k2 = kt - d;
         mbar_wait_drain(full + k2 % C::STAGES, (k2 / C::STAGES) & 1);
@@ -376,33 +404,6 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::THREADS, 1)
 }
 
 // ------------------------------------------------------------------ host
-static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-// 2-D bf16 tensor map over a row-major [rows, cols] matrix with a
-// [64 cols x box_rows] box and 128-byte swizzle.
-static bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  auto fn = get_encode();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 IndexerLayout indexer_layout(int T, int S, int max_kv, int ps) {
   IndexerLayout L{};
   const long long ch1 = kChunkDecode, ch8 = kChunkPrefill;
@@ -450,23 +451,23 @@ int run_indexer(cudaStream_t stream, const IndexerMeta& m, const uint16_t* q, co
   if (m.T == 0) return DSA_OK;
 
   CUtensorMap kmap, qmap;
-  if (!encode_bf16_2d(&kmap, kcache, (uint64_t)m.P * m.ps, 128, m.ps)) return DSA_ERR_CUDA;
-  if (!encode_bf16_2d(&qmap, q, (uint64_t)m.T * 32, 128, 32)) return DSA_ERR_CUDA;
+  if (!encode_bf16_2d(&kmap, kcache, (uint64_t)m.P * m.ps, 128, m.ps, 128)) return DSA_ERR_CUDA;
+  if (!encode_bf16_2d(&qmap, q, (uint64_t)m.T * 32, 128, 32, 128)) return DSA_ERR_CUDA;
   CUtensorMap qmap8;
-  if (!encode_bf16_2d(&qmap8, q, (uint64_t)m.T * 32, 128, 256)) return DSA_ERR_CUDA;
+  if (!encode_bf16_2d(&qmap8, q, (uint64_t)m.T * 32, 128, 256, 128)) return DSA_ERR_CUDA;
 
   indexer_plan_kernel<<<1, 1024, 0, stream>>>(m, pl, kChunkDecode, kChunkPrefill);
   DSA_CHECK_LAUNCH();
   const int sms = sm_count();
   {
     using C = IdxCfg<1>;
-    cudaFuncSetAttribute(indexer_score_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    set_smem_attr_once(reinterpret_cast<const void*>(indexer_score_kernel<1>), C::SMEM);
     indexer_score_kernel<1><<<sms, C::THREADS, C::SMEM, stream>>>(m, pl, out, kmap, qmap);
     DSA_CHECK_LAUNCH();
   }
   {
     using C = IdxCfg<8>;
-    cudaFuncSetAttribute(indexer_score_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    set_smem_attr_once(reinterpret_cast<const void*>(indexer_score_kernel<8>), C::SMEM);
     indexer_score_kernel<8><<<sms, C::THREADS, C::SMEM, stream>>>(m, pl, out, kmap, qmap8);
     DSA_CHECK_LAUNCH();
   }

@@ -16,6 +16,7 @@ namespace dsa {
 constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kTopkSmemCap = 32768;  // row elements staged in shared memory
+constexpr int kTopkSmemMax = (kTopkWarps + 1) * 256 * 4 + kTopkSmemCap * 4;
 
 // Order-preserving map fp32 -> uint32 (larger float -> larger key); -0 and +0
 // map to the same key so they tie like equal scores.
@@ -47,73 +48,76 @@ __device__ __forceinline__ int block_scan_warps(int v, int* s_tmp, int* total) {
   return r;
 }
 
-template <bool kStaged>
-__device__ void select_row(const float* __restrict__ g, const uint32_t* __restrict__ s_row, int n, int k,
-                           int32_t* __restrict__ out_idx, float* __restrict__ out_val, uint32_t* hist,
-                           int* s_tmp) {
+// Warp-aggregated histogram update: scores cluster in a few digits (the top
+// digit is the sign and high exponent bits), so lanes that share a digit add
+// once. All lanes of the warp must call it.
+__device__ __forceinline__ void hist_add(uint32_t* wh, uint32_t key, bool valid, uint32_t prefix, uint32_t mask,
+                                         int shift) {
+  const bool act = valid && (key & mask) == prefix;
+  const uint32_t bin = act ? ((key >> shift) & 255u) : 256u;
+  const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+  if (act && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(wh + bin, (uint32_t)__popc(peers));
+}
+
+// Pick the digit holding the rank-`remaining` key from the 256-bin histogram
+// (summed over warps) and update prefix / mask / remaining. Block-wide.
+__device__ __forceinline__ void pick_digit(uint32_t* hist, int shift, uint32_t& prefix, uint32_t& mask,
+                                           int& remaining, int* s_sel) {
   const int tid = threadIdx.x, w = warp_id(), lane = lane_id();
-  auto key_at = [&](int i) -> uint32_t { return kStaged ? s_row[i] : ordered_key(__ldg(g + i)); };
-  uint32_t prefix = 0, mask = 0;
-  int remaining = k;  // rank (1-based) of the wanted key among keys matching prefix
-  __shared__ int s_sel[2];
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = tid; i < kTopkWarps * 256; i += kTopkThreads) hist[i] = 0;
-    __syncthreads();
-    uint32_t* wh = hist + w * 256;
-    for (int i = tid; i < n; i += kTopkThreads) {
-      const uint32_t key = key_at(i);
-      if ((key & mask) == prefix) atomicAdd(wh + ((key >> shift) & 255u), 1u);
-    }
-    __syncthreads();
-    // reduce the per-warp histograms into hist[0..255] and pick the digit
-    if (tid < 256) {
-      uint32_t c = 0;
+  if (tid < 256) {
+    uint32_t c = 0;
 #pragma unroll
-      for (int j = 0; j < kTopkWarps; ++j) c += hist[j * 256 + tid];
-      hist[kTopkWarps * 256 + tid] = c;
-    }
-    __syncthreads();
-    if (w == 0) {
-      // suffix sums from the top digit down, 8 digits per lane
-      const uint32_t* h = hist + kTopkWarps * 256;
-      uint32_t local[8];
-      uint32_t sum = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        local[j] = h[255 - (lane * 8 + j)];
-        sum += local[j];
-      }
-      uint32_t x = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-      }
-      uint32_t above = x - sum;  // keys in digits above this lane's group
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (above < (uint32_t)remaining && above + local[j] >= (uint32_t)remaining) {
-          s_sel[0] = 255 - (lane * 8 + j);
-          s_sel[1] = (int)above;
-        }
-        above += local[j];
-      }
-    }
-    __syncthreads();
-    const uint32_t d = (uint32_t)s_sel[0];
-    remaining -= s_sel[1];
-    prefix |= d << shift;
-    mask |= 255u << shift;
-    __syncthreads();
+    for (int j = 0; j < kTopkWarps; ++j) c += hist[j * 256 + tid];
+    hist[kTopkWarps * 256 + tid] = c;
   }
-  const uint32_t kstar = prefix;
-  const int need_eq = remaining;  // copies of K* to take, lowest index first
-  // warp w owns the contiguous segment [seg0, seg1)
+  __syncthreads();
+  if (w == 0) {
+    const uint32_t* h = hist + kTopkWarps * 256;
+    uint32_t local[8];
+    uint32_t sum = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      local[j] = h[255 - (lane * 8 + j)];
+      sum += local[j];
+    }
+    uint32_t x = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    uint32_t above = x - sum;  // keys in digits above this lane's group
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (above < (uint32_t)remaining && above + local[j] >= (uint32_t)remaining) {
+        s_sel[0] = 255 - (lane * 8 + j);
+        s_sel[1] = (int)above;
+      }
+      above += local[j];
+    }
+  }
+  __syncthreads();
+  const uint32_t d = (uint32_t)s_sel[0];
+  remaining -= s_sel[1];
+  prefix |= d << shift;
+  mask |= 255u << shift;
+  __syncthreads();
+}
+
+// Ordered emission: every index with key > kstar, plus the lowest-index
+// need_eq copies of kstar, in ascending index order. Warp w owns a contiguous
+// segment; two block scans give each warp its output offset.
+template <bool kStaged>
+__device__ void emit_ordered(const float* __restrict__ g, const uint32_t* __restrict__ s_row, int n,
+                             uint32_t kstar, int need_eq, int32_t* __restrict__ out_idx, float* __restrict__ out_val,
+                             int* s_tmp) {
+  const int w = warp_id(), lane = lane_id();
+  auto key_at = [&](int i) -> uint32_t { return kStaged ? s_row[i] : ordered_key(__ldg(g + i)); };
   const int seg = ((n + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
   const int seg0 = min(n, w * seg), seg1 = min(n, seg0 + seg);
+  const int seg_end = seg1 + ((32 - (seg1 - seg0) % 32) % 32);
   int gt = 0, eq = 0;
-  for (int i = seg0 + lane; i < seg1 + ((32 - (seg1 - seg0) % 32) % 32); i += 32) {
+  for (int i = seg0 + lane; i < seg_end; i += 32) {
     const bool in = i < seg1;
     const uint32_t key = in ? key_at(i) : 0u;
     gt += __popc(__ballot_sync(0xffffffffu, in && key > kstar));
@@ -125,7 +129,7 @@ __device__ void select_row(const float* __restrict__ g, const uint32_t* __restri
   const int out_base = block_scan_warps(gt + take_eq, s_tmp, &tot);
   const uint32_t lt = (1u << lane) - 1u;
   int eq_run = eq_base, sel_run = out_base;
-  for (int i = seg0 + lane; i < seg1 + ((32 - (seg1 - seg0) % 32) % 32); i += 32) {
+  for (int i = seg0 + lane; i < seg_end; i += 32) {
     const bool in = i < seg1;
     const uint32_t key = in ? key_at(i) : 0u;
     const bool is_gt = in && key > kstar, is_eq = in && key == kstar;
@@ -136,12 +140,162 @@ __device__ void select_row(const float* __restrict__ g, const uint32_t* __restri
     if (sel) {
       const int pos = sel_run + __popc(selb & lt);
       out_idx[pos] = i;
-      if (out_val) out_val[pos] = kStaged ? __ldg(g + i) : __ldg(g + i);
+      if (out_val) out_val[pos] = __ldg(g + i);
     }
     eq_run += __popc(eqb);
     sel_run += __popc(selb);
   }
-  // k <= n here, so exactly k entries were written
+}
+
+// Bitonic sort of n_pow2 ints in shared memory (ascending), block-wide.
+__device__ void bitonic_sort_smem(int* a, int n_pow2) {
+  for (int size = 2; size <= n_pow2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < n_pow2 / 2; i += blockDim.x) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool up = (lo & size) == 0;
+        const int x = a[lo], y = a[hi];
+        if ((x > y) == up) {
+          a[lo] = y;
+          a[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+constexpr int kUnroll = 16;  // float4 loads in flight per thread on the global path
+
+// Row longer than shared memory: radix passes read it from global memory
+// (L2) with many loads in flight; the final pass collects the winners
+// unordered and sorts them.
+__device__ void select_row_global(const float* __restrict__ g, int n, int k, int32_t* __restrict__ out_idx,
+                                  float* __restrict__ out_val, uint32_t* hist, int* s_tmp, int* lists,
+                                  int list_cap) {
+  const int tid = threadIdx.x, w = warp_id();
+  uint32_t prefix = 0, mask = 0;
+  int remaining = k;
+  __shared__ int s_sel[2];
+  const float4* g4 = reinterpret_cast<const float4*>(g);
+  const int n4 = n / 4;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = tid; i < kTopkWarps * 256; i += kTopkThreads) hist[i] = 0;
+    __syncthreads();
+    uint32_t* wh = hist + w * 256;
+    for (int b0 = 0; b0 < n4; b0 += kTopkThreads * kUnroll) {
+      float4 v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int i4 = b0 + u * kTopkThreads + tid;
+        v[u] = i4 < n4 ? __ldg(g4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const bool in = b0 + u * kTopkThreads + tid < n4;
+        hist_add(wh, ordered_key(v[u].x), in, prefix, mask, shift);
+        hist_add(wh, ordered_key(v[u].y), in, prefix, mask, shift);
+        hist_add(wh, ordered_key(v[u].z), in, prefix, mask, shift);
+        hist_add(wh, ordered_key(v[u].w), in, prefix, mask, shift);
+      }
+    }
+    if (w == 0) {
+      // the < 4 tail elements (rows are not always a multiple of 4 long)
+      const int i = n4 * 4 + (tid & 31);
+      const bool in = i < n;
+      hist_add(wh, in ? ordered_key(__ldg(g + i)) : 0u, in, prefix, mask, shift);
+    }
+    __syncthreads();
+    pick_digit(hist, shift, prefix, mask, remaining, s_sel);
+  }
+  const uint32_t kstar = prefix;
+  const int need_eq = remaining;
+  const int n_gt = k - need_eq;
+  // unordered collection of the winners
+  int* s_cnt = s_tmp + 68;  // [0] greater, [1] equal
+  int* gt_list = lists;                  // list_cap entries
+  int* eq_list = lists + list_cap;       // list_cap entries
+  if (tid == 0) {
+    s_cnt[0] = 0;
+    s_cnt[1] = 0;
+  }
+  __syncthreads();
+  const uint32_t lt = (1u << (tid & 31)) - 1u;
+  for (int b0 = 0; b0 < n; b0 += kTopkThreads * 4) {
+    float vv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = b0 + u * kTopkThreads + tid;
+      vv[u] = i < n ? __ldg(g + i) : -INFINITY;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = b0 + u * kTopkThreads + tid;
+      const uint32_t key = ordered_key(vv[u]);
+      const bool in = i < n;
+      const bool is_gt = in && key > kstar, is_eq = in && key == kstar;
+      const uint32_t gb = __ballot_sync(0xffffffffu, is_gt), eb = __ballot_sync(0xffffffffu, is_eq);
+      int gbase = 0, ebase = 0;
+      if ((tid & 31) == 0) {
+        if (gb) gbase = atomicAdd(&s_cnt[0], __popc(gb));
+        if (eb) ebase = atomicAdd(&s_cnt[1], __popc(eb));
+      }
+      gbase = __shfl_sync(0xffffffffu, gbase, 0);
+      ebase = __shfl_sync(0xffffffffu, ebase, 0);
+      if (is_gt) gt_list[gbase + __popc(gb & lt)] = i;
+      if (is_eq) {
+        const int pos = ebase + __popc(eb & lt);
+        if (pos < list_cap) eq_list[pos] = i;
+      }
+    }
+  }
+  __syncthreads();
+  const int neq = s_cnt[1];
+  if (neq > list_cap || k > list_cap) {
+    // too many ties to collect: ordered emission straight from global memory
+    emit_ordered<false>(g, nullptr, n, kstar, need_eq, out_idx, out_val, s_tmp);
+    return;
+  }
+  // lowest-index need_eq ties: sort the tie list, then the k winners
+  int p2 = 1;
+  while (p2 < neq) p2 <<= 1;
+  for (int i = neq + tid; i < p2; i += kTopkThreads) eq_list[i] = 0x7fffffff;
+  __syncthreads();
+  bitonic_sort_smem(eq_list, p2);
+  for (int i = tid; i < need_eq; i += kTopkThreads) gt_list[n_gt + i] = eq_list[i];
+  int q2 = 1;
+  while (q2 < k) q2 <<= 1;
+  for (int i = k + tid; i < q2; i += kTopkThreads) gt_list[i] = 0x7fffffff;
+  __syncthreads();
+  bitonic_sort_smem(gt_list, q2);
+  for (int i = tid; i < k; i += kTopkThreads) {
+    const int idx = gt_list[i];
+    out_idx[i] = idx;
+    if (out_val) out_val[i] = __ldg(g + idx);
+  }
+}
+
+// Row staged in shared memory as ordered keys.
+__device__ void select_row_staged(const float* __restrict__ g, const uint32_t* __restrict__ s_row, int n, int k,
+                                  int32_t* __restrict__ out_idx, float* __restrict__ out_val, uint32_t* hist,
+                                  int* s_tmp) {
+  const int tid = threadIdx.x, w = warp_id();
+  uint32_t prefix = 0, mask = 0;
+  int remaining = k;
+  __shared__ int s_sel[2];
+  const int nround = (n + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = tid; i < kTopkWarps * 256; i += kTopkThreads) hist[i] = 0;
+    __syncthreads();
+    uint32_t* wh = hist + w * 256;
+    for (int i = tid; i < nround; i += kTopkThreads) hist_add(wh, i < n ? s_row[i] : 0u, i < n, prefix, mask, shift);
+    __syncthreads();
+    pick_digit(hist, shift, prefix, mask, remaining, s_sel);
+  }
+  emit_ordered<true>(g, s_row, n, prefix, remaining, out_idx, out_val, s_tmp);
 }
 
 __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const float* __restrict__ scores, long long ld,
@@ -150,8 +304,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const float* __
                                                                  float* __restrict__ out_val, int cap) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int s_tmp[72];
-  uint32_t* hist = reinterpret_cast<uint32_t*>(smem);                  // (warps + 1) * 256
-  uint32_t* s_row = hist + (kTopkWarps + 1) * 256;                      // cap keys
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem);  // (warps + 1) * 256
+  uint32_t* s_row = hist + (kTopkWarps + 1) * 256;      // cap keys
   const int row = blockIdx.x;
   int n = nvis[row];
   if (div > 1) n = (n + div - 1) / div;
@@ -166,20 +320,35 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const float* __
     return;
   }
   if (n <= cap) {
-    for (int i = threadIdx.x; i < n; i += blockDim.x) s_row[i] = ordered_key(__ldg(g + i));
+    // stage with many independent loads in flight
+    for (int b0 = 0; b0 < n; b0 += kTopkThreads * 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = b0 + u * kTopkThreads + threadIdx.x;
+        v[u] = i < n ? __ldg(g + i) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = b0 + u * kTopkThreads + threadIdx.x;
+        if (i < n) s_row[i] = ordered_key(v[u]);
+      }
+    }
     __syncthreads();
-    select_row<true>(g, s_row, n, k, oi, ov, hist, s_tmp);
+    select_row_staged(g, s_row, n, k, oi, ov, hist, s_tmp);
   } else {
-    select_row<false>(g, s_row, n, k, oi, ov, hist, s_tmp);
+    select_row_global(g, n, k, oi, ov, hist, s_tmp, reinterpret_cast<int*>(s_row), cap / 2);
   }
 }
 
 int run_topk(cudaStream_t stream, const float* scores, long long ld, const int* nvis, int T, int div, int k,
              int32_t* out_idx, float* out_val, int max_len) {
   if (T == 0) return DSA_OK;
-  const int cap = max(0, min(max_len, kTopkSmemCap));
+  // rows longer than the staging capacity use the staging area as two
+  // winner lists of cap/2 entries each
+  const int cap = max_len > kTopkSmemCap ? kTopkSmemCap : max(0, max_len);
   const size_t smem = (size_t)(kTopkWarps + 1) * 256 * 4 + (size_t)cap * 4;
-  cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  set_smem_attr_once(reinterpret_cast<const void*>(topk_rows_kernel), (int)(kTopkSmemMax));
   topk_rows_kernel<<<T, kTopkThreads, smem, stream>>>(scores, ld, nvis, div, k, out_idx, out_val, cap);
   DSA_CHECK_LAUNCH();
   return DSA_OK;
