@@ -24,6 +24,7 @@ ERRORS = {
     -5: "DSA_ERR_SHARED_BEFORE_FULL",
     -6: "DSA_ERR_BAD_INDEXER_TYPE",
     -7: "DSA_ERR_ALIGNMENT",
+    -8: "DSA_ERR_SCRATCH_LIMIT",
 }
 STATUS_UNION_TRUNCATED = 0x1
 STATUS_BAD_METADATA = 0x2
@@ -42,6 +43,7 @@ EXPORTS = (
     "dsa_sparse_mla_prefill_qblock",
     "dsa_device_sm_count",
     "dsa_launch_count",
+    "dsa_sparse_mla_decode_noalloc",
 )
 
 
@@ -82,6 +84,8 @@ def lib() -> ctypes.CDLL:
                                         _F, _P, _P, _P, _Z, _P]
     L.dsa_sparse_mla_prefill_qblock.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                                 _I, _I, _I, _I, _F, _P, _P, _P]
+    L.dsa_sparse_mla_decode_noalloc.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                                                _I, _I, _F, _P, _P, _P]
     L.dsa_device_sm_count.argtypes = []
     L.dsa_launch_count.argtypes = []
     L.dsa_launch_count.restype = ctypes.c_longlong
@@ -292,4 +296,36 @@ def dsa_sparse_mla_prefill_qblock(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_i
                                              _ptr(member), _ptr(counts), QB, u_max, T, S, P, PTW, ps, H, Dk, Dv,
                                              float(sm_scale), _ptr(o), _ptr(lse), _ptr(dev_status))
     _check("dsa_sparse_mla_prefill_qblock", rc)
+    return (o, lse) if lse is not None else o
+
+
+def dsa_sparse_mla_decode_noalloc(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, sel, *, unit, sm_scale,
+                                  o=None, lse=None, want_lse=False, dev_status=None, Dv=512):
+    """Same result as :func:`dsa_sparse_mla_decode`, without a workspace.
+
+    For callers that cannot allocate device memory on this path, for example a
+    plugin that is handed only its input and output buffers. The library keeps
+    its split scratch in a built-in 24 MiB device array. The first call on a
+    device looks up that array's address (make it before any stream capture),
+    calls that overlap on the GPU race on the array, and a problem needing more
+    scratch raises DSA_ERR_SCRATCH_LIMIT. ``o``/``lse`` may be preallocated by
+    the caller; when omitted they are allocated here with PyTorch (the library
+    call itself allocates nothing)."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev, 3)
+    _need(kv, "kv", torch.bfloat16, dev, 3)
+    _need(sel, "sel", torch.int32, dev, 2)
+    S, PTW = _meta(dev, seq_lens, cu_q_lens, cu_kv_lens, page_indices)
+    T, H, Dk = q.shape
+    P, ps, row_stride = kv.shape
+    K = sel.shape[1]
+    if o is None:
+        o = torch.empty((T, H, Dv), dtype=torch.bfloat16, device=dev)
+    if want_lse and lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    rc = lib().dsa_sparse_mla_decode_noalloc(_stream(dev), _ptr(q), _ptr(kv), row_stride, _ptr(seq_lens),
+                                             _ptr(cu_q_lens), _ptr(cu_kv_lens), _ptr(page_indices), _ptr(sel), K,
+                                             unit, T, S, P, PTW, ps, H, Dk, Dv, float(sm_scale), _ptr(o), _ptr(lse),
+                                             _ptr(dev_status))
+    _check("dsa_sparse_mla_decode_noalloc", rc)
     return (o, lse) if lse is not None else o

@@ -244,6 +244,47 @@ int dsa_sparse_mla_decode(dsa_stream_t stream, const uint16_t* q, const uint16_t
   return run_attend(static_cast<cudaStream_t>(stream), prm, ws, ws_bytes);
 }
 
+// No-allocation variant of dsa_sparse_mla_decode (declared in dsa.h): the
+// same checks and split choice; the split scratch is the library's built-in
+// device array instead of a caller workspace.
+int dsa_sparse_mla_decode_noalloc(dsa_stream_t stream, const uint16_t* q, const uint16_t* kv, int row_stride,
+                                  const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
+                                  const int32_t* page_indices, const int32_t* sel, int K, int unit, int T, int S,
+                                  int P, int PTW, int ps, int H, int Dk, int Dv, float sm_scale, uint16_t* o,
+                                  float* lse, int32_t* dev_status) {
+  int rc = check_meta(seq_lens, cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps);
+  if (rc) return rc;
+  rc = attend_check(q, kv, row_stride, T, H, Dk, Dv, o);
+  if (rc) return rc;
+  if (K < 1 || (T > 0 && !sel)) return DSA_ERR_INVALID_ARGUMENT;
+  if (unit != 1 && unit != ps) return DSA_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(sm_scale)) return DSA_ERR_INVALID_ARGUMENT;
+  if (T == 0 || H == 0) return DSA_OK;
+  AttendParams prm{};
+  prm.q = q;
+  prm.kv = kv;
+  prm.row_stride = row_stride;
+  prm.seq_lens = seq_lens;
+  prm.cu_q_lens = cu_q_lens;
+  prm.cu_kv_lens = cu_kv_lens;
+  prm.page_indices = page_indices;
+  prm.T = T;
+  prm.S = S;
+  prm.P = P;
+  prm.PTW = PTW;
+  prm.ps = ps;
+  prm.H = H;
+  prm.scale_log2 = sm_scale * 1.4426950408889634f;
+  prm.mode = unit == 1 ? kModeToken : kModePage;
+  prm.sel = sel;
+  prm.K = K;
+  prm.o = o;
+  prm.lse = lse;
+  prm.dev_status = dev_status;
+  prm.nsplit = attend_num_splits(T, H, K, prm.mode);
+  return run_attend_static_scratch(static_cast<cudaStream_t>(stream), prm);
+}
+
 int dsa_sparse_mla_prefill_qblock(dsa_stream_t stream, const uint16_t* q, const uint16_t* kv, int row_stride,
                                   const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
                                   const int32_t* page_indices, const int32_t* units, const uint32_t* member,

@@ -714,4 +714,38 @@ int run_attend(cudaStream_t stream, AttendParams prm, void* ws, size_t ws_bytes)
   return DSA_OK;
 }
 
+// ---------------------------------------------------------------------------
+// No-allocation variant of the split-key decode path. Its scratch (the split
+// partials, their lse values and the merge counters) lives in a file-scope
+// device array instead of a caller workspace, so a caller that cannot
+// allocate device memory can still run the split path. The array is part of
+// the module image: every device that loads the library holds it until the
+// process exits.
+constexpr size_t kStaticScratchBytes = 24u << 20;  // 24 MiB
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+// Device address of the array on the current device. In host code the name
+// g_static_scratch is only a host-side stand-in, so the address is resolved
+// once per device, with that device current, the first time it is needed.
+static void* static_scratch_address() {
+  static void* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+int run_attend_static_scratch(cudaStream_t stream, AttendParams prm) {
+  if (prm.T == 0 || prm.H == 0) return DSA_OK;
+  if (prm.nsplit <= 1) return run_attend(stream, prm, nullptr, 0);
+  if (attend_workspace_bytes(prm.T, prm.H, prm.nsplit) > kStaticScratchBytes) return DSA_ERR_SCRATCH_LIMIT;
+  void* p = static_scratch_address();
+  if (!p) return DSA_ERR_CUDA;
+  return run_attend(stream, prm, p, kStaticScratchBytes);
+}
+
 }  // namespace dsa

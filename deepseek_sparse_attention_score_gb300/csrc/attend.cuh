@@ -37,6 +37,8 @@ struct AttendParams {
 int attend_num_splits(int T, int H, int K, int mode);
 size_t attend_workspace_bytes(int T, int H, int nsplit);
 int run_attend(cudaStream_t stream, AttendParams prm, void* ws, size_t ws_bytes);
+// Same as run_attend with the split scratch in a built-in device array.
+int run_attend_static_scratch(cudaStream_t stream, AttendParams prm);
 
 int run_block_union(cudaStream_t stream, const int32_t* topk_units, int T, int K, int QB, int u_max,
                     const int32_t* cu_q_lens, const int32_t* cu_kv_lens, int S, int ps, int PTW, int32_t* units,

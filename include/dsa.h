@@ -62,7 +62,9 @@ enum dsa_error {
   DSA_ERR_CUDA = -4,             /* a CUDA call or kernel launch failed */
   DSA_ERR_SHARED_BEFORE_FULL = -5,
   DSA_ERR_BAD_INDEXER_TYPE = -6,
-  DSA_ERR_ALIGNMENT = -7 /* a pointer is not 16-byte aligned */
+  DSA_ERR_ALIGNMENT = -7,    /* a pointer is not 16-byte aligned */
+  DSA_ERR_SCRATCH_LIMIT = -8 /* needs more than the built-in scratch of
+                                dsa_sparse_mla_decode_noalloc (24 MiB) */
 };
 
 /* Bits OR-ed into *dev_status by the kernels. */
@@ -178,6 +180,33 @@ DSA_API int dsa_sparse_mla_decode(dsa_stream_t stream, const uint16_t* q, const 
                           const int32_t* page_indices, const int32_t* sel, int K, int unit, int T, int S, int P,
                           int PTW, int ps, int H, int Dk, int Dv, float sm_scale, uint16_t* o, float* lse,
                           void* ws, size_t ws_bytes, int32_t* dev_status);
+
+/* ------------------------------------------------------------------------
+ * Sparse MLA decode without any allocation or caller workspace.
+ * The source pages have no counterpart of this entry point. It is for
+ * callers that cannot allocate device memory on this path: for example a
+ * plugin that an inference engine hands only its input and output buffers,
+ * or code that must not allocate once it is running. It computes the same
+ * result as dsa_sparse_mla_decode (same arguments minus the workspace);
+ * when the key list is split across CTAs, the split partials live in a
+ * 24 MiB device array built into the library instead of a workspace.
+ *  - Memory: nothing is allocated. The array is part of the library image,
+ *    so every GPU that loads the library holds it until the process exits.
+ *  - Set-up: the first call on a device looks up the array's address on that
+ *    device; make that first call before any stream capture.
+ *  - Sharing: all calls use the same array and leave their last contents in
+ *    it (the merge counters are cleared on every call). Calls that overlap on
+ *    the GPU (other streams, other host threads) race on the array, so
+ *    serialise them.
+ *  - Limit: a problem whose split scratch would exceed 24 MiB returns
+ *    DSA_ERR_SCRATCH_LIMIT and enqueues nothing; use dsa_sparse_mla_decode
+ *    with a workspace for it.
+ * ------------------------------------------------------------------------ */
+DSA_API int dsa_sparse_mla_decode_noalloc(dsa_stream_t stream, const uint16_t* q, const uint16_t* kv,
+                                          int row_stride, const int32_t* seq_lens, const int32_t* cu_q_lens,
+                                          const int32_t* cu_kv_lens, const int32_t* page_indices, const int32_t* sel,
+                                          int K, int unit, int T, int S, int P, int PTW, int ps, int H, int Dk, int Dv,
+                                          float sm_scale, uint16_t* o, float* lse, int32_t* dev_status);
 
 /* ------------------------------------------------------------------------
  * Query-block sparse-MLA prefill over the block unions.
