@@ -26,6 +26,9 @@ Readings taken where the pages are silent (each is listed in the design doc):
     coincide on indices produced by the indexer);
   * a row with no valid key outputs 0 (the pages' masked softmax does the same).
 
+Queries may be given as arrays or as any mapping token -> row (so large
+batches can be checked on a sample of rows); caches are arrays.
+
 Every function here is pinned by ``tests/test_oracle_pins.py`` against values
 and properties fixed outside this file (hand-worked examples, brute force on
 tiny inputs, closed forms, reductions to library routines); none is
@@ -295,7 +298,6 @@ def sparse_mla(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, sel, unit, 
     flat = kvc.reshape(P * ps, Dk_row)
     seq = token_seq(cu_q_lens)
     nvis = visible_len(seq_lens, cu_q_lens)
-    Dk = np.asarray(q).shape[-1]
     if tokens is None:
         tokens = range(len(seq))
     os_, ls = [], []
@@ -303,7 +305,9 @@ def sparse_mla(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, sel, unit, 
         j = selected_positions(sel[t], unit, ps)
         j = j[(j >= 0) & (j < nvis[t])]
         rows = widen(flat[physical_rows(cu_kv_lens, page_indices, ps, int(seq[t]), j)])
-        o, l = _masked_softmax_attend(widen(q[t]), rows[:, :Dk], rows[:, :Dv], sm_scale)
+        qt = widen(q[t])
+        Dk = qt.shape[-1]
+        o, l = _masked_softmax_attend(qt, rows[:, :Dk], rows[:, :Dv], sm_scale)
         os_.append(o)
         ls.append(l)
     return np.stack(os_), np.stack(ls)
@@ -325,7 +329,6 @@ def qblock_attend(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, units, m
     sl = np.asarray(seq_lens, dtype=np.int64)
     pi = np.asarray(page_indices, dtype=np.int64)
     u_max = units.shape[1]
-    Dk = np.asarray(q).shape[-1]
     if tokens is None:
         tokens = range(len(seq))
     os_, ls = [], []
@@ -343,7 +346,9 @@ def qblock_attend(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, units, m
             rows_sel.append((pi[g] * ps + np.arange(ps))[ok])
         r = np.concatenate(rows_sel) if rows_sel else np.zeros(0, np.int64)
         rows = widen(flat[r])
-        o, l = _masked_softmax_attend(widen(q[t]), rows[:, :Dk], rows[:, :Dv], sm_scale)
+        qt = widen(q[t])
+        Dk = qt.shape[-1]
+        o, l = _masked_softmax_attend(qt, rows[:, :Dk], rows[:, :Dv], sm_scale)
         os_.append(o)
         ls.append(l)
     return np.stack(os_), np.stack(ls)
@@ -359,7 +364,6 @@ def dense_mla(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, sm_scale, Dv
     seq = token_seq(cu_q_lens)
     nvis = visible_len(seq_lens, cu_q_lens)
     pi = np.asarray(page_indices, dtype=np.int64)
-    Dk = np.asarray(q).shape[-1]
     if tokens is None:
         tokens = range(len(seq))
     out = []
@@ -367,6 +371,7 @@ def dense_mla(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, sm_scale, Dv
         s = int(seq[t])
         qt = widen(q[t])
         H = qt.shape[0]
+        Dk = qt.shape[-1]
         n = int(nvis[t])
         if n == 0:
             out.append(np.zeros((H, Dv)))
