@@ -126,6 +126,16 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def measured_tensor_peak():
+    """Dense bf16 peak: the burst figure, since stages are timed alone."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d["bf16_tflops"], "measured (burst)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def committed_traffic(kernel_key):
     """DRAM bytes per launch from a committed ncu summary, only while the
     kernel source is unchanged since the counters were taken."""
@@ -139,6 +149,49 @@ def committed_traffic(kernel_key):
         return d["bytes_per_launch"] if h == d["source_sha256_16"] else None
     except Exception:
         return None
+
+
+def stage_roofline(wl, rn, timed):
+    """Time every stage of one layer in isolation (L2 flushed before each)
+    and set its algorithmic work against the roofline it is bound by:
+    decode indexer 256 B per visible key and decode attention 1152 B per
+    selected visible key (HBM); prefill indexer 2*32*128 FLOP per visible
+    (query, key) pair and query-block attention 2*H*(576+512) FLOP per
+    (query, selected visible key) pair (tensor, bf16)."""
+    import numpy as np
+    import torch
+
+    rg = wl.rg
+    hbm, hbm_kind = measured_peaks()
+    tfl, tfl_kind = measured_tensor_peak()
+    nvis = np.clip(np.minimum(rg.seq_lens[rg.token_seq()], rg.token_pos() + 1), 0, None).astype(np.int64)
+    out = {}
+
+    def entry(ms, work, bound):
+        if bound == "hbm":
+            ach = work / (ms * 1e-3) / 1e9
+            return {"ms": ms, "algorithmic_bytes": int(work), "bound": "hbm", "achieved": ach, "unit": "GB/s",
+                    "peak": hbm, "peak_kind": hbm_kind, "frac": ach / hbm}
+        ach = work / (ms * 1e-3) / 1e12
+        return {"ms": ms, "algorithmic_flops": int(work), "bound": "tensor", "achieved": ach, "unit": "TFLOP/s",
+                "peak": tfl, "peak_kind": tfl_kind, "frac": ach / tfl}
+
+    ps = rg.page_size
+    if rn.prefill or rn.page_budget is not None:
+        tp = rn.topk_pages[0].cpu().numpy().astype(np.int64)
+        keys = np.where(tp >= 0, np.clip(nvis[:, None] - tp * ps, 0, ps), 0).sum()
+    else:
+        keys = int((rn.topk[0] >= 0).sum().item())
+    if rn.prefill:
+        out["indexer_page_topk"] = entry(timed(lambda: rn.index(0)), 2 * 32 * 128 * nvis.sum(), "tensor")
+        out["block_union"] = entry(timed(lambda: rn.union(0)), rn.topk_pages[0].numel() * 4, "hbm")
+        out["sparse_mla_prefill_qblock"] = entry(timed(lambda: rn.attend(0)), 2 * wl.H * (576 + 512) * keys,
+                                                 "tensor")
+    else:
+        name = "indexer_page_topk" if rn.page_budget is not None else "indexer_topk"
+        out[name] = entry(timed(lambda: rn.index(0)), 256 * nvis.sum(), "hbm")
+        out["sparse_mla_decode"] = entry(timed(lambda: rn.attend(0)), 1152 * keys, "hbm")
+    return out
 
 
 # ---------------------------------------------------------------- oracle leg
@@ -338,42 +391,33 @@ def run_ours(args):
             ts.append(a.elapsed_time(b))
         return statistics.median(ts)
 
-    t_index = timed(lambda: rn.index(0))
-    t_attend = timed(lambda: rn.attend(0))
-    nvis = torch.from_numpy(np.minimum(wl.rg.seq_lens, 1 << 30).astype(np.int64))
-    keys_indexed = int(nvis.sum())  # decode: every visible key once
-    sel_valid = int((rn.topk[0] >= 0).sum().item())
-    peak, peak_kind = measured_peaks()
-    att_bytes = sel_valid * 1152
-    idx_bytes = keys_indexed * 256
-    kern = {
-        "sparse_mla_decode": {"ms": t_attend, "algorithmic_bytes": att_bytes,
-                              "gbs": att_bytes / (t_attend * 1e-3) / 1e9},
-        "indexer_topk": {"ms": t_index, "algorithmic_bytes": idx_bytes, "gbs": idx_bytes / (t_index * 1e-3) / 1e9},
-    }
-    dom = "sparse_mla_decode" if t_attend >= t_index else "indexer_topk"
-    ach = kern[dom]["gbs"]
-    roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-            "peak_kind": peak_kind, "traffic": committed_traffic(dom)}
+    kern = stage_roofline(wl, rn, timed)
+    dom = max(kern, key=lambda k: kern[k]["ms"])
+    d = kern[dom]
+    roof = {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"], "unit": d["unit"],
+            "frac": d["frac"], "peak_kind": d["peak_kind"], "traffic": committed_traffic(dom)}
 
     # end to end through the public API with host buffers
     pin = lambda t: t.detach().to("cpu").pin_memory()
-    h_q_idx, h_w, h_q = pin(rn.q_idx), pin(rn.w), pin(rn.q[0])
+    h_q_idx, h_w = pin(rn.q_idx), pin(rn.w)
+    h_q = [pin(x) for x in rn.q]
     h_meta = [pin(m) for m in rn.meta]
     h_topk = torch.empty(rn.topk[0].shape, dtype=torch.int32).pin_memory()
-    h_o = torch.empty(rn.o[0].shape, dtype=torch.bfloat16).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in [h_q_idx, h_w, h_q, *h_meta])
-    d2h = h_topk.numel() * 4 + h_o.numel() * 2
+    h_o = [torch.empty(x.shape, dtype=torch.bfloat16).pin_memory() for x in rn.o]
+    h2d = sum(t.numel() * t.element_size() for t in [h_q_idx, h_w, *h_q, *h_meta])
+    d2h = h_topk.numel() * 4 + sum(x.numel() * 2 for x in h_o)
 
     def e2e_step():
         rn.q_idx.copy_(h_q_idx, non_blocking=True)
         rn.w.copy_(h_w, non_blocking=True)
-        rn.q[0].copy_(h_q, non_blocking=True)
+        for d, h in zip(rn.q, h_q):
+            d.copy_(h, non_blocking=True)
         for d, h in zip(rn.meta, h_meta):
             d.copy_(h, non_blocking=True)
         rn.step()
         h_topk.copy_(rn.topk[0], non_blocking=True)
-        h_o.copy_(rn.o[0], non_blocking=True)
+        for h, d in zip(h_o, rn.o):
+            h.copy_(d, non_blocking=True)
 
     for _ in range(args.warmup):
         e2e_step()
@@ -396,7 +440,8 @@ def run_ours(args):
            "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * e2e_s / args.steps}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    decode_workload = not rn.prefill and rn.page_budget is None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and decode_workload:
         v, dt, ntok, nreq = time_oracle(wl)
         cpu = {"value": v, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
                "sample": f"{nreq} requests of the {args.workload} workload taken in order ({ntok} decode "
@@ -408,6 +453,7 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": args.workload, "requests": wl.rg.S, "tokens_per_step": T,
+                       "layers": len(rn.types),
                        "kv_len": "U{4096..8192}" if args.workload == "batched_decode" else "see DESIGN.md",
                        "k": wl.k, "mla_heads": wl.H, "page_size": wl.rg.page_size,
                        "l2": "flushed (512 MB write) before every timed step", "cuda_graph": graph is not None,
