@@ -47,6 +47,25 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(seconds, world):
+    """The slowest rank's time (replicas are timed independently; the job
+    takes as long as its slowest replica). Uses the default process group."""
+    if world <= 1:
+        return seconds
+    import torch
+    import torch.distributed as tdist
+
+    t = torch.tensor([seconds], dtype=torch.float64)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(tokens_per_step, steps, world, seconds):
+    """Whole-job tokens/s of ``world`` replicas that each ran ``steps`` steps
+    of ``tokens_per_step`` tokens in at most ``seconds``."""
+    return tokens_per_step * steps * world / seconds
+
+
 # ----------------------------------------------------------------- helpers
 def blas_threads():
     """Threads of the BLAS numpy runs the oracle's matmuls on."""
@@ -370,12 +389,8 @@ def run_ours(args):
                 run()
             torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    total_s = sum(step_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([total_s], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_s = float(t.item())
-    value = T * args.steps * world / total_s
+    total_s = max_over_ranks(sum(step_ms) / 1e3, world)
+    value = replica_throughput(T, args.steps, world, total_s)
     clocks = clk.summary()
 
     # per-ABI-call times (eager, L2 flushed before each) for the roofline
@@ -431,12 +446,8 @@ def run_ours(args):
         b.record()
         torch.cuda.synchronize()
         e_ms.append(a.elapsed_time(b))
-    e2e_s = sum(e_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([e2e_s], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = {"value": T * args.steps * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+    e2e_s = max_over_ranks(sum(e_ms) / 1e3, world)
+    e2e = {"value": replica_throughput(T, args.steps, world, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * e2e_s / args.steps}
 
     cpu = None
