@@ -2,24 +2,30 @@
 // query-block form of sparse_mla_prefill_qblock.py, _qblock_kernel).
 //
 // One CTA computes one query token x up to 128 heads x one half of the
-// 512-wide latent value. Per 32-key tile:
-//   S[128 heads x 32 keys] = Q[128 x 576] * K_tile[32 x 576]^T   (TMEM, fp32)
+// 512-wide latent value. Per 64-key tile:
+//   S[128 heads x 64 keys] = Q[128 x 576] * K_tile[64 x 576]^T   (TMEM, fp32)
 //   online softmax over the keys, in registers, one head per thread
-//   O[128 x 256] += P[128 x 32] * V_tile[32 x 256]              (TMEM, fp32)
+//   O[128 x 256] += P[128 x 64] * V_tile[64 x 256]              (TMEM, fp32)
 // O of all 512 value columns would fill the whole 512-column TMEM, leaving no
 // room for S, so the value width is split across two CTAs that both form S
 // (the pair reads the same keys; the second read is an L2 hit).
 //
-// Q[:, 0:448] is kept in TMEM and feeds QK^T as the A operand (tcgen05 "TS"
-// form), which keeps shared memory free for five KV stages and removes most
-// of the A-operand shared-memory traffic; Q[:, 448:576] stays in shared
-// memory. Keys are gathered row by row (1152 bytes each) with cp.async into
-// the ring of 128-byte-swizzled column blocks; the same bytes serve as the
-// K-major B operand of QK^T and as the MN-major B operand of PV. One warp
-// walks the key list ahead of the gather and prefetches the rows into L2.
-// Key lists come from (a) token top-k rows, (b) page top-k rows, or (c) a
-// query block's union + membership bitmap (qblock form). Masked keys are
-// zero-filled and get probability 0.
+// A tcgen05.mma with M = 128 and K = 16 costs about the same for every N up
+// to 64, so keys are multiplied 64 at a time: a 32-key tile would leave the
+// tensor pipe idle half of the time. Q[:, 0:384] is kept in TMEM and feeds
+// QK^T as the A operand (tcgen05 "TS" form); Q[:, 384:576] stays in shared
+// memory. Each key tile is stored as nine 128-byte-swizzled column blocks of
+// 64 dims; the same bytes are the K-major B operand of QK^T and the MN-major
+// B operand of PV. The four blocks holding this CTA's value half (the
+// "V part") are only released once PV has read them; the other five (the
+// "K part") as soon as QK^T has. QK^T runs over the K part first, then PV of
+// the previous tile, then the V part, so the tensor pipe never waits for the
+// softmax and a V part has most of two tiles of time to arrive.
+//
+// Keys are resolved 32 at a time by one warp (token top-k rows, page top-k
+// rows, or a query block's union + membership bitmap); runs of 32
+// consecutive rows of one page are fetched with 2-D TMA boxes, scattered
+// rows with coalesced cp.async. Masked keys are zero-filled or carry P = 0.
 #include "common.cuh"
 #include "attend.cuh"
 
@@ -30,34 +36,45 @@ namespace {
 constexpr int kThreads = 384;
 constexpr int kCopyWarps = 6;
 constexpr int kCopyThreads = kCopyWarps * 32;
-constexpr int kTileKeys = 32;
-constexpr int kStages = 5;   // KV tiles resident in shared memory
-constexpr int kRing = 8;     // key-address tiles generated (and L2-prefetched) ahead of the gather
+constexpr int kSubKeys = 32;   // keys resolved / copied per generator step
+constexpr int kTileKeys = 64;  // keys per MMA tile (two generator steps)
+constexpr int kRing = 8;       // generator steps buffered ahead of the gather
 constexpr int kDk = 576, kDv = 512, kDvHalf = 256;
-constexpr int kQTmemDims = 448;  // Q[:, 0:448] lives in TMEM (224 columns), Q[:, 448:576] in smem
-constexpr int kQTmemSteps = kQTmemDims / 16;  // 28 of the 36 K-steps read A from TMEM
-constexpr int kQsBytes = 128 * (kDk - kQTmemDims) * 2;  // 32768: 2 column blocks x 16 KB
-constexpr int kStageBytes = kTileKeys * kDk * 2;        // 36864: 9 column blocks x 4 KB
-constexpr int kPBytes = 128 * kTileKeys * 2;            // 8192
+constexpr int kBlk = kTileKeys * 128;   // one 64-dim column block of a tile: 8 KB
+constexpr int kKBlocks = 5, kVBlocks = 4;
+constexpr int kKStages = 2, kVStages = 2;
+constexpr int kKStageBytes = kKBlocks * kBlk;  // 40960
+constexpr int kVStageBytes = kVBlocks * kBlk;  // 32768
+constexpr int kQTmemBlocks = 6;                // Q column blocks 0..5 in TMEM (192 columns)
+constexpr int kQTmemDims = kQTmemBlocks * 64;  // 384
+constexpr int kQsBytes = (kDk - kQTmemDims) / 64 * 16384;  // 3 column blocks x 16 KB
+constexpr int kPBytes = 128 * kTileKeys * 2;               // 16 KB, 128-byte swizzled K-major
 constexpr int OFF_QS = 0;
-constexpr int OFF_ST = OFF_QS + kQsBytes;
-constexpr int OFF_P = OFF_ST + kStages * kStageBytes;
-constexpr int OFF_RING = OFF_P + kPBytes;         // int32 [kRing][32] physical rows
-constexpr int OFF_RINFO = OFF_RING + kRing * 32 * 4;  // uint32 mask[kRing], end[kRing]
-constexpr int OFF_RBASE = OFF_RINFO + kRing * 8;      // int32 base row of contiguous tiles [kRing]
-constexpr int OFF_SINFO = OFF_RBASE + kRing * 4;      // uint32 mask[kStages], end[kStages]
-constexpr int OFF_BAR = (OFF_SINFO + kStages * 8 + 7) & ~7;
-constexpr int NBAR = 2 * kStages + 2 * kRing + 5;
+constexpr int OFF_P = OFF_QS + kQsBytes;
+constexpr int OFF_KST = OFF_P + kPBytes;
+constexpr int OFF_VST = OFF_KST + kKStages * kKStageBytes;
+constexpr int OFF_RING = OFF_VST + kVStages * kVStageBytes;  // int32 [kRing][32] physical rows
+constexpr int OFF_RINFO = OFF_RING + kRing * 32 * 4;         // uint32 mask[kRing], end[kRing]
+constexpr int OFF_RBASE = OFF_RINFO + kRing * 8;             // int32 base row of contiguous steps [kRing]
+constexpr int OFF_SINFO = OFF_RBASE + kRing * 4;  // uint32 kend[kKStages], vmask[kVStages][2], vend[kVStages]
+constexpr int OFF_BAR = (OFF_SINFO + (kKStages + 3 * kVStages) * 4 + 7) & ~7;
+constexpr int NBAR = 2 * kKStages + 2 * kVStages + 2 * kRing + 5;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int kSmem = OFF_MISC + 16;
+static_assert(kSmem <= 227 * 1024, "shared memory budget");
+static_assert(OFF_P % 1024 == 0 && OFF_KST % 1024 == 0 && OFF_VST % 1024 == 0, "swizzle atoms need 1 KB alignment");
 constexpr uint32_t kIdescQK = make_idesc_bf16(128, kTileKeys, false, false);
 constexpr uint32_t kIdescPV = make_idesc_bf16(128, kDvHalf, false, true);
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColQ = 0;    // 224 columns of packed bf16 pairs
-constexpr uint32_t kColS = 224;  // 32 fp32 columns
+constexpr uint32_t kColQ = 0;    // 192 columns of packed bf16 pairs
+constexpr uint32_t kColS = 192;  // 64 fp32 columns
 constexpr uint32_t kColO = 256;  // 256 fp32 columns
 constexpr float kRescaleThreshold = 8.f;  // log2 units: p stays <= 256
 constexpr int kMaxSplits = 8;
+// every full barrier completes after two generator steps' worth of arrivals:
+// each gather thread once per step, plus one more by the leader per step
+constexpr uint32_t kFullArrivals = 2 * (kCopyThreads + 1);
+
 }  // namespace
 
 // Warp-wide generator of 32-key tiles. Every lane gets the flat physical row
@@ -170,10 +187,10 @@ struct TileGen {
       mask = m;
       return true;
     }
-    const int tiles_per_unit = ps / kTileKeys;
+    const int tiles_per_unit = ps / kSubKeys;
     while (true) {
       if (cur_valid && sub < tiles_per_unit) {
-        const int k0 = sub * kTileKeys + lane;
+        const int k0 = sub * kSubKeys + lane;
         bool v;
         if (mode == kModePage) {
           v = cur_key0 + k0 < n_vis;
@@ -181,7 +198,7 @@ struct TileGen {
           const int kp = cur_key0 + k0;  // kp = g*ps + r - base_tok
           v = kp <= pos && kp < kv_len;
         }
-        base = (long long)cur_phys * ps + sub * kTileKeys;
+        base = (long long)cur_phys * ps + sub * kSubKeys;
         ++sub;
         row = v ? (long long)cur_phys * ps + k0 : -1;
         mask = __ballot_sync(0xffffffffu, v);
@@ -225,6 +242,87 @@ struct TileGen {
   }
 };
 
+// The MMA issuer (one thread). Every operand descriptor is a base register
+// plus a compile-time offset, so issuing an MMA costs a couple of
+// instructions: a single thread that has to build descriptors, branch and
+// wait on dependent integer ops between MMAs cannot keep the tensor pipe fed
+// at these small N. The value half is a template argument for that reason.
+struct MmaBars {
+  uint64_t *kfull, *kempty, *vfull, *vempty, *sfull, *sempty, *pfull, *pempty, *fin;
+};
+
+template <int HALF>
+__device__ __forceinline__ void mma_issuer(uint32_t tmem, uint32_t qs_addr, uint32_t p_addr, uint32_t kst_addr,
+                                           uint32_t vst_addr, const MmaBars& br, volatile uint32_t* kst_end,
+                                           volatile int* abort_flag) {
+  const uint64_t dq = make_sdesc(qs_addr, 16, 1024, kSwizzle128B);
+  const uint64_t dp = make_sdesc(p_addr, 16, 1024, kSwizzle128B);
+  const uint64_t dk[2] = {make_sdesc(kst_addr, 16, 1024, kSwizzle128B),
+                          make_sdesc(kst_addr + kKStageBytes, 16, 1024, kSwizzle128B)};
+  const uint64_t dv[2] = {make_sdesc(vst_addr, 16, 1024, kSwizzle128B),
+                          make_sdesc(vst_addr + kVStageBytes, 16, 1024, kSwizzle128B)};
+  // the V part as the MN-major B operand of PV: 64-column blocks kBlk apart
+  const uint64_t dvn[2] = {make_sdesc(vst_addr, kBlk, 1024, kSwizzle128B),
+                           make_sdesc(vst_addr + kVStageBytes, kBlk, 1024, kSwizzle128B)};
+  static_assert(kKStages == 2 && kVStages == 2, "stage selection below assumes two stages");
+  const uint32_t tS = tmem + kColS, tO = tmem + kColO, tQ = tmem + kColQ;
+  // descriptors address shared memory in 16-byte units in their low bits
+  auto qk_block = [&](const int c, const uint64_t b0, const bool first) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint64_t b = b0 + (uint64_t)((kk * 32) >> 4);
+      const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+      if (c < kQTmemBlocks)
+        umma_bf16_ts(tS, tQ + c * 32 + kk * 8, b, kIdescQK, acc);
+      else
+        umma_bf16_ss(tS, dq + (uint64_t)(((c - kQTmemBlocks) * 16384 + kk * 32) >> 4), b, kIdescQK, acc);
+    }
+  };
+  bool ok = true;
+  int issued = 0;
+  for (int i = 0;; ++i) {
+    const int ks = i & 1, vs = i & 1;
+    if (!(ok = mbar_wait(br.kfull + ks, (i >> 1) & 1, abort_flag))) break;
+    const bool end = kst_end[ks] != 0;
+    if (!end) {
+      fence_proxy_async_smem();  // cp.async data -> async proxy
+      // single S buffer: the softmax must have read S(i-1)
+      if (i > 0 && !(ok = mbar_wait(br.sempty, (i - 1) & 1, abort_flag))) break;
+      tc_fence_after();
+      const uint64_t kb = ks ? dk[1] : dk[0];
+#pragma unroll
+      for (int pos = 0; pos < kKBlocks; ++pos)
+        qk_block(HALF == 0 ? 4 + pos : (pos < 4 ? pos : 8), kb + (uint64_t)((pos * kBlk) >> 4), pos == 0);
+      umma_commit(br.kempty + ks);
+      issued = 1;
+    }
+    if (i > 0) {
+      if (!(ok = mbar_wait(br.pfull, (i - 1) & 1, abort_flag))) break;
+      tc_fence_after();
+      const int pvs = (i - 1) & 1;
+      const uint64_t vb = pvs ? dvn[1] : dvn[0];
+#pragma unroll
+      for (int k2 = 0; k2 < kTileKeys / 16; ++k2)
+        umma_bf16_ss(tO, dp + (uint64_t)((k2 * 32) >> 4), vb + (uint64_t)((k2 * 16 * 128) >> 4), kIdescPV,
+                     (i > 1 || k2 > 0) ? 1u : 0u);
+      umma_commit(br.vempty + pvs);
+      umma_commit(br.pempty);
+    }
+    if (end) break;
+    if (!(ok = mbar_wait(br.vfull + vs, (i >> 1) & 1, abort_flag))) break;
+    fence_proxy_async_smem();
+    tc_fence_after();
+    const uint64_t vb = vs ? dv[1] : dv[0];
+#pragma unroll
+    for (int pos = 0; pos < kVBlocks; ++pos) qk_block(4 * HALF + pos, vb + (uint64_t)((pos * kBlk) >> 4), false);
+    umma_commit(br.sfull);
+  }
+  if (!ok && issued) {
+    umma_commit(br.fin);
+    mbar_wait_drain(br.fin, 0);
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_mla_kernel(const AttendParams prm, const __grid_constant__ CUtensorMap kvmap) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -237,19 +335,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t = blockIdx.y, split = blockIdx.z;
   const int h0 = hg * 128;
   uint8_t* qs_s = smem + OFF_QS;
-  uint8_t* st_s = smem + OFF_ST;
   uint8_t* p_s = smem + OFF_P;
+  uint8_t* kst_s = smem + OFF_KST;
+  uint8_t* vst_s = smem + OFF_VST;
   int* ring_rows = reinterpret_cast<int*>(smem + OFF_RING);
   volatile uint32_t* ring_mask = reinterpret_cast<volatile uint32_t*>(smem + OFF_RINFO);
   volatile uint32_t* ring_end = ring_mask + kRing;
   volatile int* ring_base = reinterpret_cast<volatile int*>(smem + OFF_RBASE);
-  volatile uint32_t* st_mask = reinterpret_cast<volatile uint32_t*>(smem + OFF_SINFO);
-  volatile uint32_t* st_end = st_mask + kStages;
+  volatile uint32_t* kst_end = reinterpret_cast<volatile uint32_t*>(smem + OFF_SINFO);
+  volatile uint32_t* vst_mask = kst_end + kKStages;   // [kVStages][2]
+  volatile uint32_t* vst_end = vst_mask + 2 * kVStages;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint64_t* full = bars;                  // [kStages] 64 async + 1 leader arrivals
-  uint64_t* empty = bars + kStages;       // [kStages] PV commit
-  uint64_t* rfull = bars + 2 * kStages;   // [kRing] generator
-  uint64_t* rempty = rfull + kRing;       // [kRing] 64 gather threads
+  uint64_t* kfull = bars;                 // [kKStages] kFullArrivals + tx bytes
+  uint64_t* kempty = kfull + kKStages;    // [kKStages] commit after the K-part MMAs
+  uint64_t* vfull = kempty + kKStages;    // [kVStages] kFullArrivals + tx bytes
+  uint64_t* vempty = vfull + kVStages;    // [kVStages] commit after PV
+  uint64_t* rfull = vempty + kVStages;    // [kRing] generator
+  uint64_t* rempty = rfull + kRing;       // [kRing] gather threads
   uint64_t* sfull = rempty + kRing;       // QK commit
   uint64_t* sempty = sfull + 1;           // 128 softmax threads
   uint64_t* pfull = sfull + 2;            // 128 softmax threads
@@ -259,9 +361,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(full + i, kCopyThreads + 1);
-      mbar_init(empty + i, 1);
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(kfull + i, kFullArrivals);
+      mbar_init(kempty + i, 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(vfull + i, kFullArrivals);
+      mbar_init(vempty + i, 1);
     }
     for (int i = 0; i < kRing; ++i) {
       mbar_init(rfull + i, 1);
@@ -281,12 +387,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int nh = min(128, prm.H - h0);
   const uint16_t* qt = prm.q + ((size_t)t * prm.H + h0) * kDk;
-  // Q[:, 448:576] -> two 128-byte-swizzled column blocks in shared memory;
-  // Q[:, 0:448] staged row-major (912-byte rows, conflict-free 16-byte reads)
-  // in the still unused KV ring, then moved into TMEM by the softmax warps.
+  // Q[:, 384:576] -> three 128-byte-swizzled column blocks in shared memory;
+  // Q[:, 0:384] staged row-major (784-byte rows, conflict-free 16-byte reads)
+  // in the still unused key stages, then moved into TMEM by the softmax warps.
   constexpr int kQRowStage = kQTmemDims * 2 + 16;
+  static_assert(128 * kQRowStage <= kKStages * kKStageBytes + kVStages * kVStageBytes, "Q staging fits");
+  uint8_t* qstage = kst_s;
   // The key generator (warp 1) resolves its first window of selections while
-  // the other warps stage Q; it publishes tiles only after the barrier below.
+  // the other warps stage Q; it publishes steps only after the barrier below.
   TileGen gen;
   bool gen_more = false;
   long long gen_row = -1, gen_base = -1;
@@ -295,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gen.init(prm, t, split);
     gen_more = gen.next(gen_row, gen_mask, gen_base);
   } else {
-    const uint32_t qbase = smem_u32(qs_s), stage = smem_u32(st_s);
+    const uint32_t qbase = smem_u32(qs_s), stage = smem_u32(qstage);
     constexpr int CH = kDk / 8;  // 72 chunks of 16 bytes per row
     const int qtid = tid < 32 ? tid : tid - 32;  // warp 1 is busy generating keys
     for (int c = qtid; c < 128 * CH; c += kThreads - 32) {
@@ -318,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= 4 && warp < 8) {
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint4* src = reinterpret_cast<const uint4*>(st_s + r * kQRowStage);
+    const uint4* src = reinterpret_cast<const uint4*>(qstage + r * kQRowStage);
 #pragma unroll 1
     for (int c0 = 0; c0 < kQTmemDims / 2; c0 += 32) {
       uint32_t v[32];
@@ -341,133 +449,160 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t qsaddr = smem_u32(qs_s), paddr = smem_u32(p_s);
-      auto issue_qk = [&](int i) {
-        const uint32_t kaddr = smem_u32(st_s + (i % kStages) * kStageBytes);
-#pragma unroll 4
-        for (int kk = 0; kk < kQTmemSteps; ++kk) {
-          const uint64_t b = make_sdesc(kaddr + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
-          umma_bf16_ts(tmem + kColS, tmem + kColQ + kk * 8, b, kIdescQK, kk > 0);
-        }
-#pragma unroll
-        for (int kk = kQTmemSteps; kk < kDk / 16; ++kk) {
-          const int k2 = kk - kQTmemSteps;
-          const uint64_t a = make_sdesc(qsaddr + (k2 >> 2) * 16384 + (k2 & 3) * 32, 16, 1024, kSwizzle128B);
-          const uint64_t b = make_sdesc(kaddr + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
-          umma_bf16_ss(tmem + kColS, a, b, kIdescQK, 1u);
-        }
-        umma_commit(sfull);
-      };
-      auto issue_pv = [&](int i) {
-        const int s = i % kStages;
-        const uint32_t vaddr = smem_u32(st_s + s * kStageBytes) + half * 4 * 4096;
-#pragma unroll
-        for (int ks = 0; ks < kTileKeys / 16; ++ks) {
-          const uint64_t a = make_sdesc(paddr + ks * 2 * 128, 128, 512, kSwizzleNone);
-          const uint64_t b = make_sdesc(vaddr + ks * 16 * 128, 4096, 1024, kSwizzle128B);
-          umma_bf16_ss(tmem + kColO, a, b, kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
-        }
-        umma_commit(empty + s);
-        umma_commit(pempty);
-      };
-      bool ok = mbar_wait(full + 0, 0, abort_flag);
-      int issued = 0;
-      if (ok && !st_end[0]) {
-        fence_proxy_async_smem();  // cp.async data -> async proxy
-        tc_fence_after();
-        issue_qk(0);
-        issued = 1;
-        for (int i = 0;; ++i) {
-          const int s1 = (i + 1) % kStages;
-          if (!(ok = mbar_wait(full + s1, ((i + 1) / kStages) & 1, abort_flag))) break;
-          const bool end1 = st_end[s1] != 0;
-          if (!end1) {
-            fence_proxy_async_smem();
-            // single S buffer: softmax must have read S(i)
-            if (!(ok = mbar_wait(sempty, i & 1, abort_flag))) break;
-            tc_fence_after();
-            issue_qk(i + 1);
-          }
-          if (!(ok = mbar_wait(pfull, i & 1, abort_flag))) break;
-          tc_fence_after();
-          issue_pv(i);
-          if (end1) break;
-        }
-      }
-      if (!ok && issued) {
-        umma_commit(fin);
-        mbar_wait_drain(fin, 0);
-      }
+      const MmaBars br{kfull, kempty, vfull, vempty, sfull, sempty, pfull, pempty, fin};
+      if (half == 0)
+        mma_issuer<0>(tmem, smem_u32(qs_s), smem_u32(p_s), smem_u32(kst_s), smem_u32(vst_s), br, kst_end, abort_flag);
+      else
+        mma_issuer<1>(tmem, smem_u32(qs_s), smem_u32(p_s), smem_u32(kst_s), smem_u32(vst_s), br, kst_end, abort_flag);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ key generator
-    for (int j = 0;; ++j) {
-      long long row = gen_row, base = gen_base;
-      uint32_t mask = gen_mask;
-      const bool more = j == 0 ? gen_more : gen.next(row, mask, base);
+    // Steps are published in pairs (one MMA tile); a list that ends after an
+    // odd number of steps gets one empty step (no keys) to complete its tile.
+    int j = 0;
+    auto publish = [&](long long row, uint32_t mask, long long base, bool end) -> bool {
       const int slot = j % kRing;
       int ok = 1;
       if (lane == 0) ok = mbar_wait(rempty + slot, ((j / kRing) & 1) ^ 1, abort_flag) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      ring_rows[slot * 32 + lane] = more ? (int)row : -1;
+      if (!ok) return false;
+      ring_rows[slot * 32 + lane] = end ? -1 : (int)row;
       if (lane == 0) {
-        ring_mask[slot] = mask;
-        ring_end[slot] = more ? 0u : 1u;
-        ring_base[slot] = more ? (int)base : -1;
+        ring_mask[slot] = end ? 0u : mask;
+        ring_end[slot] = end ? 1u : 0u;
+        ring_base[slot] = end ? -1 : (int)base;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(rfull + slot);
+      ++j;
+      return true;
+    };
+    for (bool first = true;; first = false) {
+      long long row = gen_row, base = gen_base;
+      uint32_t mask = gen_mask;
+      const bool more = first ? gen_more : gen.next(row, mask, base);
+      if (!more && (j & 1)) {
+        if (!publish(-1, 0u, -1, false)) break;
+      }
+      if (!publish(row, mask, base, !more)) break;
       if (!more) break;
     }
   } else if (warp < 4 || warp >= 8) {
     // ------------------------------------------------------------ gather
+    // Tile by tile (two generator steps): the K parts of both steps as soon
+    // as the K stage is free, then the V parts once PV has released the V
+    // stage, so a K part is never held up behind the V stage.
     const int cw = warp < 4 ? warp - 2 : warp - 6;  // 0..5
     const int ctid = cw * 32 + lane;
-    const uint32_t stbase = smem_u32(st_s);
-    for (int i = 0;; ++i) {
-      const int slot = i % kRing, s = i % kStages;
-      if (!mbar_wait(rfull + slot, (i / kRing) & 1, abort_flag)) break;
-      const bool end = ring_end[slot] != 0;
-      const uint32_t mask = ring_mask[slot];
-      if (!mbar_wait(empty + s, ((i / kStages) & 1) ^ 1, abort_flag)) break;
-      const int cbase = ring_base[slot];
-      if (!end && cbase >= 0) {
-        // 32 consecutive rows of one page: nine 2-D TMA boxes (64 cols x 32 rows)
+    // scattered rows: copier warp cw copies keys cw, cw+6, ... of a step; per
+    // key the K part is 40 16-byte chunks (lanes 0..31, then 0..7 again) and
+    // the V part 32 (one per lane), each a contiguous run of the row
+    const int kc1 = lane + 32;
+    const int kpos0 = lane >> 3, kpos1 = kc1 >> 3;
+    const int kcol0 = half == 0 ? 4 + kpos0 : kpos0;            // kpos0 < 4
+    const int kcol1 = half == 0 ? 4 + kpos1 : (kpos1 < 4 ? kpos1 : 8);
+    const int vcol = 4 * half + (lane >> 3);
+    const int src_k0 = kcol0 * 64 + (lane & 7) * 8, src_k1 = kcol1 * 64 + (kc1 & 7) * 8;
+    const int src_v = vcol * 64 + (lane & 7) * 8;
+    const uint32_t dst_k0 = kpos0 * kBlk, dst_k1 = kpos1 * kBlk, dst_v = (lane >> 3) * kBlk;
+    for (int ti = 0;; ++ti) {
+      const int j0 = 2 * ti, s0 = j0 % kRing, s1 = (j0 + 1) % kRing;
+      const int ks = ti % kKStages, vs = ti % kVStages;
+      if (!mbar_wait(rfull + s0, (j0 / kRing) & 1, abort_flag)) break;
+      if (ring_end[s0]) {
+        // the end marker stands for a whole tile: both steps' arrivals
+        if (!mbar_wait(kempty + ks, ((ti / kKStages) & 1) ^ 1, abort_flag)) break;
+        if (!mbar_wait(vempty + vs, ((ti / kVStages) & 1) ^ 1, abort_flag)) break;
         if (ctid == 0) {
-          uint8_t* dst = st_s + s * kStageBytes;
-          mbar_arrive_expect_tx(full + s, kStageBytes);
+          kst_end[ks] = 1u;
+          vst_end[vs] = 1u;
+          mbar_arrive(kfull + ks);
+          mbar_arrive(vfull + vs);
+          mbar_arrive(kfull + ks);
+          mbar_arrive(vfull + vs);
+        }
+        mbar_arrive(kfull + ks);
+        mbar_arrive(vfull + vs);
+        mbar_arrive(kfull + ks);
+        mbar_arrive(vfull + vs);
+        mbar_arrive(rempty + s0);
+        break;
+      }
+      if (!mbar_wait(rfull + s1, ((j0 + 1) / kRing) & 1, abort_flag)) break;
+      const int base0 = ring_base[s0], base1 = ring_base[s1];
+      // ---- K parts
+      if (!mbar_wait(kempty + ks, ((ti / kKStages) & 1) ^ 1, abort_flag)) break;
+      const uint32_t kd = smem_u32(kst_s + ks * kKStageBytes);
 #pragma unroll 1
-          for (int c = 0; c < kDk / 64; ++c) tma_load_2d(dst + c * 4096, &kvmap, full + s, c * 64, cbase);
-        } else {
-          mbar_arrive(full + s);
-        }
-      } else if (!end) {
-        // scattered rows: copier warp cw copies keys cw, cw+6, ...; per key three
-        // coalesced 512-byte instructions (chunks lane, lane+32, lane+64 of 72)
-        const uint32_t dst0 = stbase + s * kStageBytes;
-#pragma unroll 2
-        for (int key = cw; key < kTileKeys; key += kCopyWarps) {
-          const int r = ring_rows[slot * 32 + key];
-          const uint16_t* rb = r >= 0 ? prm.kv + (size_t)r * prm.row_stride : prm.kv;
-          const uint32_t nb = r >= 0 ? 16u : 0u;
-#pragma unroll
-          for (int part = 0; part < 3; ++part) {
-            const int ch = lane + 32 * part;
-            if (ch < 72) cp_async16(dst0 + (ch >> 3) * 4096 + sw128_offset(key, ch & 7), rb + ch * 8, nb);
+      for (int sb = 0; sb < 2; ++sb) {
+        const int slot = sb ? s1 : s0, cbase = sb ? base1 : base0;
+        const uint32_t d = kd + sb * (kSubKeys * 128);
+        if (cbase >= 0) {
+          // 32 consecutive rows of one page: one 2-D TMA box (64 cols x 32 rows) per block
+          if (ctid == 0) {
+            mbar_arrive_expect_tx(kfull + ks, kKBlocks * kSubKeys * 128);
+#pragma unroll 1
+            for (int pos = 0; pos < kKBlocks; ++pos) {
+              const int c = half == 0 ? 4 + pos : (pos < 4 ? pos : 8);
+              tma_load_2d(kst_s + ks * kKStageBytes + sb * (kSubKeys * 128) + pos * kBlk, &kvmap, kfull + ks,
+                          c * 64, cbase);
+            }
+          } else {
+            mbar_arrive(kfull + ks);
           }
+        } else {
+#pragma unroll 2
+          for (int key = cw; key < kSubKeys; key += kCopyWarps) {
+            const int r = ring_rows[slot * 32 + key];
+            const uint16_t* rb = r >= 0 ? prm.kv + (size_t)r * prm.row_stride : prm.kv;
+            const uint32_t nb = r >= 0 ? 16u : 0u;
+            cp_async16(d + dst_k0 + sw128_offset(key, lane & 7), rb + src_k0, nb);
+            if (lane < 8) cp_async16(d + dst_k1 + sw128_offset(key, kc1 & 7), rb + src_k1, nb);
+          }
+          cp_async_mbar_arrive_noinc(kfull + ks);
         }
-        cp_async_mbar_arrive_noinc(full + s);
-      } else {
-        mbar_arrive(full + s);
       }
       if (ctid == 0) {
-        st_mask[s] = mask;
-        st_end[s] = end ? 1u : 0u;
-        mbar_arrive(full + s);
+        kst_end[ks] = 0u;
+        mbar_arrive(kfull + ks);
+        mbar_arrive(kfull + ks);
       }
-      mbar_arrive(rempty + slot);
-      if (end) break;
+      // ---- V parts
+      if (!mbar_wait(vempty + vs, ((ti / kVStages) & 1) ^ 1, abort_flag)) break;
+      const uint32_t vd = smem_u32(vst_s + vs * kVStageBytes);
+#pragma unroll 1
+      for (int sb = 0; sb < 2; ++sb) {
+        const int slot = sb ? s1 : s0, cbase = sb ? base1 : base0;
+        const uint32_t d = vd + sb * (kSubKeys * 128);
+        if (cbase >= 0) {
+          if (ctid == 0) {
+            mbar_arrive_expect_tx(vfull + vs, kVBlocks * kSubKeys * 128);
+#pragma unroll 1
+            for (int pos = 0; pos < kVBlocks; ++pos)
+              tma_load_2d(vst_s + vs * kVStageBytes + sb * (kSubKeys * 128) + pos * kBlk, &kvmap, vfull + vs,
+                          (4 * half + pos) * 64, cbase);
+          } else {
+            mbar_arrive(vfull + vs);
+          }
+        } else {
+#pragma unroll 2
+          for (int key = cw; key < kSubKeys; key += kCopyWarps) {
+            const int r = ring_rows[slot * 32 + key];
+            const uint16_t* rb = r >= 0 ? prm.kv + (size_t)r * prm.row_stride : prm.kv;
+            cp_async16(d + dst_v + sw128_offset(key, lane & 7), rb + src_v, r >= 0 ? 16u : 0u);
+          }
+          cp_async_mbar_arrive_noinc(vfull + vs);
+        }
+      }
+      if (ctid == 0) {
+        vst_mask[2 * vs] = ring_mask[s0];
+        vst_mask[2 * vs + 1] = ring_mask[s1];
+        vst_end[vs] = 0u;
+        mbar_arrive(vfull + vs);
+        mbar_arrive(vfull + vs);
+      }
+      mbar_arrive(rempty + s0);
+      mbar_arrive(rempty + s1);
     }
     cp_async_wait<0>();
   } else {
@@ -479,39 +614,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     int n = 0;
     bool ok = true;
     for (int i = 0;; ++i) {
-      const int s = i % kStages;
-      if (!(ok = mbar_wait(full + s, (i / kStages) & 1, abort_flag))) break;
-      if (st_end[s]) break;
-      const uint32_t mask = st_mask[s];
+      const int vs = i % kVStages;
+      if (!(ok = mbar_wait(vfull + vs, (i / kVStages) & 1, abort_flag))) break;
+      if (vst_end[vs]) break;
+      const uint32_t mlo = vst_mask[2 * vs], mhi = vst_mask[2 * vs + 1];
       if (!(ok = mbar_wait(sfull, i & 1, abort_flag))) break;
       tc_fence_after();
-      uint32_t sv[32];
-      tmem_ld32(tmem + lane_base + kColS, sv);
+      uint32_t sa[32], sb[32];
+      tmem_ld32(tmem + lane_base + kColS, sa);
+      tmem_ld32(tmem + lane_base + kColS + 32, sb);
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(sempty);
-      float x[32];
+      // scaled, masked logits in place (log2 units)
       float mt = -INFINITY;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        x[j] = ((mask >> j) & 1u) ? __uint_as_float(sv[j]) * sl2 : -INFINITY;
-        mt = fmaxf(mt, x[j]);
+        const float a = ((mlo >> j) & 1u) ? __uint_as_float(sa[j]) * sl2 : -INFINITY;
+        const float b = ((mhi >> j) & 1u) ? __uint_as_float(sb[j]) * sl2 : -INFINITY;
+        sa[j] = __float_as_uint(a);
+        sb[j] = __float_as_uint(b);
+        mt = fmaxf(mt, fmaxf(a, b));
       }
       const float m_new = fmaxf(m_run, mt);
       const bool need = m_new > m_run + kRescaleThreshold;  // also true when m_run == -inf
       const float m_use = need ? m_new : m_run;
       const float alpha = need ? exp2f(m_run - m_new) : 1.f;
-      float psum = 0.f;
-      uint32_t pk[16];
-#pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        const float p0 = exp2f(x[j] - m_use), p1 = exp2f(x[j + 1] - m_use);
-        psum += p0 + p1;
-        __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-        pk[j >> 1] = *reinterpret_cast<uint32_t*>(&b2);
-      }
-      l_run = l_run * alpha + psum;
-      m_run = m_use;
+      // P(i) overwrites P(i-1): PV(i-1) must have read it (and be done with O)
       if (i > 0) {
         if (!(ok = mbar_wait(pempty, (i - 1) & 1, abort_flag))) break;
         tc_fence_after();
@@ -528,11 +657,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st_wait();
         }
       }
-      // P row -> no-swizzle K-major core matrices: (r/8)*512 + (j/8)*128 + (r%8)*16
-      uint8_t* prow = p_s + (r >> 3) * 512 + (r & 7) * 16;
+      // P row r (bf16) -> 128-byte-swizzled K-major layout, one 16-byte chunk
+      // of 8 keys at a time, so no 64-entry array stays live
+      float psum = 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4*>(prow + c * 128) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int j = (c & 3) * 8 + 2 * q;
+          const float x0 = __uint_as_float(c < 4 ? sa[j] : sb[j]);
+          const float x1 = __uint_as_float(c < 4 ? sa[j + 1] : sb[j + 1]);
+          const float p0 = ex2_approx(x0 - m_use), p1 = ex2_approx(x1 - m_use);
+          psum += p0 + p1;
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+          w[q] = *reinterpret_cast<uint32_t*>(&b2);
+        }
+        *reinterpret_cast<uint4*>(p_s + sw128_offset(r, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      l_run = l_run * alpha + psum;
+      m_run = m_use;
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(pfull);
