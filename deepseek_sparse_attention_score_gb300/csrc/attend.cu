@@ -38,7 +38,7 @@ constexpr int kCopyWarps = 6;
 constexpr int kCopyThreads = kCopyWarps * 32;
 constexpr int kSubKeys = 32;   // keys resolved / copied per generator step
 constexpr int kTileKeys = 64;  // keys per MMA tile (two generator steps)
-constexpr int kRing = 8;       // generator steps buffered ahead of the gather
+constexpr int kRing = 12;      // generator steps buffered ahead of the gather
 constexpr int kDk = 576, kDv = 512, kDvHalf = 256;
 constexpr int kBlk = kTileKeys * 128;   // one 64-dim column block of a tile: 8 KB
 constexpr int kKBlocks = 5, kVBlocks = 4;
@@ -481,6 +481,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       long long row = gen_row, base = gen_base;
       uint32_t mask = gen_mask;
       const bool more = first ? gen_more : gen.next(row, mask, base);
+      // decode rows come from all over HBM: start pulling this step's rows
+      // into L2 now, a whole ring ahead of the gather (union pages of a query
+      // block are shared by its queries and are L2-resident anyway)
+      if (more && row >= 0 && prm.mode != kModeQblock) {
+        const char* rp = reinterpret_cast<const char*>(prm.kv + (size_t)row * prm.row_stride);
+#pragma unroll
+        for (int l = 0; l < kDk * 2 / 128; ++l) prefetch_l2_line(rp + l * 128);
+      }
       if (!more && (j & 1)) {
         if (!publish(-1, 0u, -1, false)) break;
       }
@@ -626,16 +634,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(sempty);
-      // scaled, masked logits in place (log2 units)
-      float mt = -INFINITY;
+      // scaled, masked logits in place (log2 units); independent partial
+      // maxima keep the dependency chains short
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if ((mlo & mhi) == 0xffffffffu) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float a = ((mlo >> j) & 1u) ? __uint_as_float(sa[j]) * sl2 : -INFINITY;
-        const float b = ((mhi >> j) & 1u) ? __uint_as_float(sb[j]) * sl2 : -INFINITY;
-        sa[j] = __float_as_uint(a);
-        sb[j] = __float_as_uint(b);
-        mt = fmaxf(mt, fmaxf(a, b));
+        for (int j = 0; j < 32; ++j) {
+          const float a = __uint_as_float(sa[j]) * sl2, b = __uint_as_float(sb[j]) * sl2;
+          sa[j] = __float_as_uint(a);
+          sb[j] = __float_as_uint(b);
+          mx4[j & 1] = fmaxf(mx4[j & 1], a);
+          mx4[2 + (j & 1)] = fmaxf(mx4[2 + (j & 1)], b);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float a = ((mlo >> j) & 1u) ? __uint_as_float(sa[j]) * sl2 : -INFINITY;
+          const float b = ((mhi >> j) & 1u) ? __uint_as_float(sb[j]) * sl2 : -INFINITY;
+          sa[j] = __float_as_uint(a);
+          sb[j] = __float_as_uint(b);
+          mx4[j & 1] = fmaxf(mx4[j & 1], a);
+          mx4[2 + (j & 1)] = fmaxf(mx4[2 + (j & 1)], b);
+        }
       }
+      const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       const float m_new = fmaxf(m_run, mt);
       const bool need = m_new > m_run + kRescaleThreshold;  // also true when m_run == -inf
       const float m_use = need ? m_new : m_run;
@@ -659,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // P row r (bf16) -> 128-byte-swizzled K-major layout, one 16-byte chunk
       // of 8 keys at a time, so no 64-entry array stays live
-      float psum = 0.f;
+      float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         uint32_t w[4];
@@ -669,12 +691,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float x0 = __uint_as_float(c < 4 ? sa[j] : sb[j]);
           const float x1 = __uint_as_float(c < 4 ? sa[j + 1] : sb[j + 1]);
           const float p0 = ex2_approx(x0 - m_use), p1 = ex2_approx(x1 - m_use);
-          psum += p0 + p1;
+          ps4[q] += p0 + p1;
           __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
           w[q] = *reinterpret_cast<uint32_t*>(&b2);
         }
         *reinterpret_cast<uint4*>(p_s + sw128_offset(r, c)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
+      const float psum = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
       l_run = l_run * alpha + psum;
       m_run = m_use;
       fence_proxy_async_smem();
