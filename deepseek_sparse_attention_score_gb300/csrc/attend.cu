@@ -12,15 +12,15 @@
 //
 // A tcgen05.mma with M = 128 and K = 16 costs about the same for every N up
 // to 64, so keys are multiplied 64 at a time: a 32-key tile would leave the
-// tensor pipe idle half of the time. Q[:, 0:384] is kept in TMEM and feeds
-// QK^T as the A operand (tcgen05 "TS" form); Q[:, 384:576] stays in shared
-// memory. Each key tile is stored as nine 128-byte-swizzled column blocks of
-// 64 dims; the same bytes are the K-major B operand of QK^T and the MN-major
-// B operand of PV. The four blocks holding this CTA's value half (the
-// "V part") are only released once PV has read them; the other five (the
-// "K part") as soon as QK^T has. QK^T runs over the K part first, then PV of
-// the previous tile, then the V part, so the tensor pipe never waits for the
-// softmax and a V part has most of two tiles of time to arrive.
+// tensor pipe idle half of the time. Q[:, 0:256] is kept in TMEM and feeds
+// QK^T as the A operand (tcgen05 "TS" form); Q[:, 256:576] stays in shared
+// memory. S is double-buffered in TMEM and the softmax writes P (bf16) back
+// over its S buffer, where PV reads it as a TS-form A operand, so QK^T of the
+// next tile never waits for the softmax. Each key tile is stored as nine
+// 128-byte-swizzled column blocks of 64 dims; the same bytes are the K-major
+// B operand of QK^T and the MN-major B operand of PV. The four blocks holding
+// this CTA's value half (the "V part") are only released once PV has read
+// them; the other five (the "K part") as soon as QK^T has.
 //
 // Keys are resolved 32 at a time by one warp (token top-k rows, page top-k
 // rows, or a query block's union + membership bitmap); runs of 32
@@ -45,29 +45,27 @@ constexpr int kKBlocks = 5, kVBlocks = 4;
 constexpr int kKStages = 2, kVStages = 2;
 constexpr int kKStageBytes = kKBlocks * kBlk;  // 40960
 constexpr int kVStageBytes = kVBlocks * kBlk;  // 32768
-constexpr int kQTmemBlocks = 6;                // Q column blocks 0..5 in TMEM (192 columns)
-constexpr int kQTmemDims = kQTmemBlocks * 64;  // 384
-constexpr int kQsBytes = (kDk - kQTmemDims) / 64 * 16384;  // 3 column blocks x 16 KB
-constexpr int kPBytes = 128 * kTileKeys * 2;               // 16 KB, 128-byte swizzled K-major
+constexpr int kQTmemBlocks = 4;                // Q column blocks 0..3 in TMEM (128 columns)
+constexpr int kQTmemDims = kQTmemBlocks * 64;  // 256
+constexpr int kQsBytes = (kDk - kQTmemDims) / 64 * 16384;  // 5 column blocks x 16 KB
 constexpr int OFF_QS = 0;
-constexpr int OFF_P = OFF_QS + kQsBytes;
-constexpr int OFF_KST = OFF_P + kPBytes;
+constexpr int OFF_KST = OFF_QS + kQsBytes;
 constexpr int OFF_VST = OFF_KST + kKStages * kKStageBytes;
 constexpr int OFF_RING = OFF_VST + kVStages * kVStageBytes;  // int32 [kRing][32] physical rows
 constexpr int OFF_RINFO = OFF_RING + kRing * 32 * 4;         // uint32 mask[kRing], end[kRing]
 constexpr int OFF_RBASE = OFF_RINFO + kRing * 8;             // int32 base row of contiguous steps [kRing]
 constexpr int OFF_SINFO = OFF_RBASE + kRing * 4;  // uint32 kend[kKStages], vmask[kVStages][2], vend[kVStages]
 constexpr int OFF_BAR = (OFF_SINFO + (kKStages + 3 * kVStages) * 4 + 7) & ~7;
-constexpr int NBAR = 2 * kKStages + 2 * kVStages + 2 * kRing + 5;
+constexpr int NBAR = 2 * kKStages + 2 * kVStages + 2 * kRing + 6;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int kSmem = OFF_MISC + 16;
 static_assert(kSmem <= 227 * 1024, "shared memory budget");
-static_assert(OFF_P % 1024 == 0 && OFF_KST % 1024 == 0 && OFF_VST % 1024 == 0, "swizzle atoms need 1 KB alignment");
+static_assert(OFF_KST % 1024 == 0 && OFF_VST % 1024 == 0, "swizzle atoms need 1 KB alignment");
 constexpr uint32_t kIdescQK = make_idesc_bf16(128, kTileKeys, false, false);
 constexpr uint32_t kIdescPV = make_idesc_bf16(128, kDvHalf, false, true);
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColQ = 0;    // 192 columns of packed bf16 pairs
-constexpr uint32_t kColS = 192;  // 64 fp32 columns
+constexpr uint32_t kColQ = 0;    // 128 columns of packed bf16 pairs
+constexpr uint32_t kColS = 128;  // two S buffers of 64 fp32 columns; P (bf16 pairs) overwrites S
 constexpr uint32_t kColO = 256;  // 256 fp32 columns
 constexpr float kRescaleThreshold = 8.f;  // log2 units: p stays <= 256
 constexpr int kMaxSplits = 8;
@@ -91,7 +89,7 @@ struct TileGen {
   // token mode: buffered tiles
   int buf_row[GB];
   uint32_t buf_mask[GB];
-  int buf_n, buf_i;
+  uint32_t buf_pend;  // windows of the buffer with keys, not returned yet
   // page / qblock modes: current window
   uint32_t pend;      // units of the window still to visit
   int w_key0;         // this lane's unit: first key position (page) or kp base (qblock)
@@ -111,7 +109,7 @@ struct TileGen {
     kv_len = g.kv_len;
     n_vis = g.n_vis;
     page_base = g.page_base;
-    buf_n = buf_i = 0;
+    buf_pend = 0;
     pend = 0;
     sub = 0;
     cur_valid = 0;
@@ -149,7 +147,7 @@ struct TileGen {
     const int ps = p->ps;
     base = -1;
     if (mode == kModeToken) {
-      while (buf_i == buf_n) {
+      while (!buf_pend) {
         if (e >= e1) return false;
         int j[GB];
 #pragma unroll
@@ -160,29 +158,28 @@ struct TileGen {
         int pg[GB];
 #pragma unroll
         for (int g = 0; g < GB; ++g) pg[g] = (j[g] >= 0 && j[g] < n_vis) ? page_of(page_base + j[g] / ps) : -1;
-        buf_n = buf_i = 0;
+        // every array index below is a compile-time constant, so the buffer
+        // stays in registers
 #pragma unroll
         for (int g = 0; g < GB; ++g) {
           const bool v = pg[g] >= 0;
           const uint32_t m = __ballot_sync(0xffffffffu, v);
-          if (m) {
-            buf_row[buf_n] = v ? pg[g] * ps + j[g] % ps : -1;
-            buf_mask[buf_n] = m;
-            ++buf_n;
-          }
+          buf_row[g] = v ? pg[g] * ps + j[g] % ps : -1;
+          buf_mask[g] = m;
+          buf_pend |= (m ? 1u : 0u) << g;
         }
         e += 32 * GB;
       }
-      // registers are indexed dynamically here; GB is small
+      const int gsel = __ffs(buf_pend) - 1;
+      buf_pend &= buf_pend - 1u;
       int r = -1;
       uint32_t m = 0;
 #pragma unroll
       for (int g = 0; g < GB; ++g)
-        if (g == buf_i) {
+        if (g == gsel) {
           r = buf_row[g];
           m = buf_mask[g];
         }
-      ++buf_i;
       row = r;
       mask = m;
       return true;
@@ -247,16 +244,19 @@ struct TileGen {
 // instructions: a single thread that has to build descriptors, branch and
 // wait on dependent integer ops between MMAs cannot keep the tensor pipe fed
 // at these small N. The value half is a template argument for that reason.
+//
+// Order per tile i: QK^T(i) over the K part, then over the V part (into S
+// buffer i % 2), then PV(i-1) with P(i-1) read from TMEM. With two S buffers
+// QK^T(i) never waits for the softmax of tile i-1, whose TMEM read of S
+// takes on the order of a thousand cycles to land.
 struct MmaBars {
-  uint64_t *kfull, *kempty, *vfull, *vempty, *sfull, *sempty, *pfull, *pempty, *fin;
+  uint64_t *kfull, *kempty, *vfull, *vempty, *sfull, *pfull, *pempty, *fin;
 };
 
 template <int HALF>
-__device__ __forceinline__ void mma_issuer(uint32_t tmem, uint32_t qs_addr, uint32_t p_addr, uint32_t kst_addr,
-                                           uint32_t vst_addr, const MmaBars& br, volatile uint32_t* kst_end,
-                                           volatile int* abort_flag) {
+__device__ __forceinline__ void mma_issuer(uint32_t tmem, uint32_t qs_addr, uint32_t kst_addr, uint32_t vst_addr,
+                                           const MmaBars& br, volatile uint32_t* kst_end, volatile int* abort_flag) {
   const uint64_t dq = make_sdesc(qs_addr, 16, 1024, kSwizzle128B);
-  const uint64_t dp = make_sdesc(p_addr, 16, 1024, kSwizzle128B);
   const uint64_t dk[2] = {make_sdesc(kst_addr, 16, 1024, kSwizzle128B),
                           make_sdesc(kst_addr + kKStageBytes, 16, 1024, kSwizzle128B)};
   const uint64_t dv[2] = {make_sdesc(vst_addr, 16, 1024, kSwizzle128B),
@@ -265,9 +265,9 @@ __device__ __forceinline__ void mma_issuer(uint32_t tmem, uint32_t qs_addr, uint
   const uint64_t dvn[2] = {make_sdesc(vst_addr, kBlk, 1024, kSwizzle128B),
                            make_sdesc(vst_addr + kVStageBytes, kBlk, 1024, kSwizzle128B)};
   static_assert(kKStages == 2 && kVStages == 2, "stage selection below assumes two stages");
-  const uint32_t tS = tmem + kColS, tO = tmem + kColO, tQ = tmem + kColQ;
+  const uint32_t tO = tmem + kColO, tQ = tmem + kColQ;
   // descriptors address shared memory in 16-byte units in their low bits
-  auto qk_block = [&](const int c, const uint64_t b0, const bool first) {
+  auto qk_block = [&](const uint32_t tS, const int c, const uint64_t b0, const bool first) {
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const uint64_t b = b0 + (uint64_t)((kk * 32) >> 4);
@@ -285,37 +285,39 @@ __device__ __forceinline__ void mma_issuer(uint32_t tmem, uint32_t qs_addr, uint
     if (!(ok = mbar_wait(br.kfull + ks, (i >> 1) & 1, abort_flag))) break;
     const bool end = kst_end[ks] != 0;
     if (!end) {
+      // S buffer i % 2 last held P(i-2), which PV(i-2) (issued before this
+      // point, and the tensor pipe runs in order) has read
+      const uint32_t tS = tmem + kColS + (uint32_t)(i & 1) * kTileKeys;
       fence_proxy_async_smem();  // cp.async data -> async proxy
-      // single S buffer: the softmax must have read S(i-1)
-      if (i > 0 && !(ok = mbar_wait(br.sempty, (i - 1) & 1, abort_flag))) break;
       tc_fence_after();
       const uint64_t kb = ks ? dk[1] : dk[0];
 #pragma unroll
       for (int pos = 0; pos < kKBlocks; ++pos)
-        qk_block(HALF == 0 ? 4 + pos : (pos < 4 ? pos : 8), kb + (uint64_t)((pos * kBlk) >> 4), pos == 0);
+        qk_block(tS, HALF == 0 ? 4 + pos : (pos < 4 ? pos : 8), kb + (uint64_t)((pos * kBlk) >> 4), pos == 0);
       umma_commit(br.kempty + ks);
       issued = 1;
+      if (!(ok = mbar_wait(br.vfull + vs, (i >> 1) & 1, abort_flag))) break;
+      fence_proxy_async_smem();
+      tc_fence_after();
+      const uint64_t vb = vs ? dv[1] : dv[0];
+#pragma unroll
+      for (int pos = 0; pos < kVBlocks; ++pos)
+        qk_block(tS, 4 * HALF + pos, vb + (uint64_t)((pos * kBlk) >> 4), false);
+      umma_commit(br.sfull + (i & 1));
     }
     if (i > 0) {
-      if (!(ok = mbar_wait(br.pfull, (i - 1) & 1, abort_flag))) break;
+      const int j = i - 1;
+      if (!(ok = mbar_wait(br.pfull + (j & 1), (j >> 1) & 1, abort_flag))) break;
       tc_fence_after();
-      const int pvs = (i - 1) & 1;
-      const uint64_t vb = pvs ? dvn[1] : dvn[0];
+      const uint32_t tP = tmem + kColS + (uint32_t)(j & 1) * kTileKeys;  // P(j): 32 columns of bf16 pairs
+      const uint64_t vb = (j & 1) ? dvn[1] : dvn[0];
 #pragma unroll
       for (int k2 = 0; k2 < kTileKeys / 16; ++k2)
-        umma_bf16_ss(tO, dp + (uint64_t)((k2 * 32) >> 4), vb + (uint64_t)((k2 * 16 * 128) >> 4), kIdescPV,
-                     (i > 1 || k2 > 0) ? 1u : 0u);
-      umma_commit(br.vempty + pvs);
+        umma_bf16_ts(tO, tP + k2 * 8, vb + (uint64_t)((k2 * 16 * 128) >> 4), kIdescPV, (j > 0 || k2 > 0) ? 1u : 0u);
+      umma_commit(br.vempty + (j & 1));
       umma_commit(br.pempty);
     }
     if (end) break;
-    if (!(ok = mbar_wait(br.vfull + vs, (i >> 1) & 1, abort_flag))) break;
-    fence_proxy_async_smem();
-    tc_fence_after();
-    const uint64_t vb = vs ? dv[1] : dv[0];
-#pragma unroll
-    for (int pos = 0; pos < kVBlocks; ++pos) qk_block(4 * HALF + pos, vb + (uint64_t)((pos * kBlk) >> 4), false);
-    umma_commit(br.sfull);
   }
   if (!ok && issued) {
     umma_commit(br.fin);
@@ -335,7 +337,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t = blockIdx.y, split = blockIdx.z;
   const int h0 = hg * 128;
   uint8_t* qs_s = smem + OFF_QS;
-  uint8_t* p_s = smem + OFF_P;
   uint8_t* kst_s = smem + OFF_KST;
   uint8_t* vst_s = smem + OFF_VST;
   int* ring_rows = reinterpret_cast<int*>(smem + OFF_RING);
@@ -352,11 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* vempty = vfull + kVStages;    // [kVStages] commit after PV
   uint64_t* rfull = vempty + kVStages;    // [kRing] generator
   uint64_t* rempty = rfull + kRing;       // [kRing] gather threads
-  uint64_t* sfull = rempty + kRing;       // QK commit
-  uint64_t* sempty = sfull + 1;           // 128 softmax threads
-  uint64_t* pfull = sfull + 2;            // 128 softmax threads
-  uint64_t* pempty = sfull + 3;           // PV commit
-  uint64_t* fin = sfull + 4;
+  uint64_t* sfull = rempty + kRing;       // [2] QK^T commit, one per S buffer
+  uint64_t* pfull = sfull + 2;            // [2] 128 softmax threads (P written over S)
+  uint64_t* pempty = sfull + 4;           // PV commit
+  uint64_t* fin = sfull + 5;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
@@ -374,8 +374,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(rempty + i, kCopyThreads);
     }
     mbar_init(sfull, 1);
-    mbar_init(sempty, 128);
+    mbar_init(sfull + 1, 1);
     mbar_init(pfull, 128);
+    mbar_init(pfull + 1, 128);
     mbar_init(pempty, 1);
     mbar_init(fin, 1);
     *abort_flag = 0;
@@ -387,8 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int nh = min(128, prm.H - h0);
   const uint16_t* qt = prm.q + ((size_t)t * prm.H + h0) * kDk;
-  // Q[:, 384:576] -> three 128-byte-swizzled column blocks in shared memory;
-  // Q[:, 0:384] staged row-major (784-byte rows, conflict-free 16-byte reads)
+  // Q[:, 256:576] -> five 128-byte-swizzled column blocks in shared memory;
+  // Q[:, 0:256] staged row-major (528-byte rows, conflict-free 16-byte reads)
   // in the still unused key stages, then moved into TMEM by the softmax warps.
   constexpr int kQRowStage = kQTmemDims * 2 + 16;
   static_assert(128 * kQRowStage <= kKStages * kKStageBytes + kVStages * kVStageBytes, "Q staging fits");
@@ -449,11 +450,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const MmaBars br{kfull, kempty, vfull, vempty, sfull, sempty, pfull, pempty, fin};
+      const MmaBars br{kfull, kempty, vfull, vempty, sfull, pfull, pempty, fin};
       if (half == 0)
-        mma_issuer<0>(tmem, smem_u32(qs_s), smem_u32(p_s), smem_u32(kst_s), smem_u32(vst_s), br, kst_end, abort_flag);
+        mma_issuer<0>(tmem, smem_u32(qs_s), smem_u32(kst_s), smem_u32(vst_s), br, kst_end, abort_flag);
       else
-        mma_issuer<1>(tmem, smem_u32(qs_s), smem_u32(p_s), smem_u32(kst_s), smem_u32(vst_s), br, kst_end, abort_flag);
+        mma_issuer<1>(tmem, smem_u32(qs_s), smem_u32(kst_s), smem_u32(vst_s), br, kst_end, abort_flag);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ key generator
@@ -626,14 +627,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = mbar_wait(vfull + vs, (i / kVStages) & 1, abort_flag))) break;
       if (vst_end[vs]) break;
       const uint32_t mlo = vst_mask[2 * vs], mhi = vst_mask[2 * vs + 1];
-      if (!(ok = mbar_wait(sfull, i & 1, abort_flag))) break;
+      if (!(ok = mbar_wait(sfull + (i & 1), (i >> 1) & 1, abort_flag))) break;
       tc_fence_after();
+      const uint32_t tS = tmem + lane_base + kColS + (uint32_t)(i & 1) * kTileKeys;
       uint32_t sa[32], sb[32];
-      tmem_ld32(tmem + lane_base + kColS, sa);
-      tmem_ld32(tmem + lane_base + kColS + 32, sb);
+      tmem_ld32(tS, sa);
+      tmem_ld32(tS + 32, sb);
       tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(sempty);
       // scaled, masked logits in place (log2 units); independent partial
       // maxima keep the dependency chains short
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -662,47 +662,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool need = m_new > m_run + kRescaleThreshold;  // also true when m_run == -inf
       const float m_use = need ? m_new : m_run;
       const float alpha = need ? exp2f(m_run - m_new) : 1.f;
-      // P(i) overwrites P(i-1): PV(i-1) must have read it (and be done with O)
-      if (i > 0) {
+      // rescaling O must wait until PV(i-1) has added into it; P(i) goes to
+      // the other S buffer than P(i-1), so without a rescale nothing waits
+      if (i > 0 && __any_sync(0xffffffffu, need)) {
         if (!(ok = mbar_wait(pempty, (i - 1) & 1, abort_flag))) break;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) {
 #pragma unroll 1
-          for (int c = 0; c < kDvHalf / 32; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(tmem + lane_base + kColO + c * 32, ov);
-            tmem_ld_wait();
+        for (int c = 0; c < kDvHalf / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_base + kColO + c * 32, ov);
+          tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
-            tmem_st32(tmem + lane_base + kColO + c * 32, ov);
-          }
-          tmem_st_wait();
+          for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+          tmem_st32(tmem + lane_base + kColO + c * 32, ov);
         }
+        tmem_st_wait();
       }
-      // P row r (bf16) -> 128-byte-swizzled K-major layout, one 16-byte chunk
-      // of 8 keys at a time, so no 64-entry array stays live
+      // P row r as bf16 pairs (lower key in the low half) over the first 32
+      // columns of its S buffer: the A operand of PV in the tcgen05 TS form
       float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pw[32];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t w[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int j = (c & 3) * 8 + 2 * q;
-          const float x0 = __uint_as_float(c < 4 ? sa[j] : sb[j]);
-          const float x1 = __uint_as_float(c < 4 ? sa[j + 1] : sb[j + 1]);
-          const float p0 = ex2_approx(x0 - m_use), p1 = ex2_approx(x1 - m_use);
-          ps4[q] += p0 + p1;
-          __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-          w[q] = *reinterpret_cast<uint32_t*>(&b2);
-        }
-        *reinterpret_cast<uint4*>(p_s + sw128_offset(r, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+      for (int c = 0; c < 32; ++c) {
+        const float x0 = __uint_as_float(c < 16 ? sa[2 * c] : sb[2 * c - 32]);
+        const float x1 = __uint_as_float(c < 16 ? sa[2 * c + 1] : sb[2 * c - 31]);
+        const float p0 = ex2_approx(x0 - m_use), p1 = ex2_approx(x1 - m_use);
+        ps4[c & 3] += p0 + p1;
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+        pw[c] = *reinterpret_cast<uint32_t*>(&b2);
       }
+      tmem_st32(tS, pw);
+      tmem_st_wait();
       const float psum = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
       l_run = l_run * alpha + psum;
       m_run = m_use;
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(pfull);
+      mbar_arrive(pfull + (i & 1));
       n = i + 1;
     }
     // epilogue
@@ -785,9 +780,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mx = fmaxf(mx, wz[z]);
         }
         float tot = 0.f;
-        for (int z = 0; z < prm.nsplit; ++z) {
-          wz[z] = (mx == -INFINITY || wz[z] == -INFINITY) ? 0.f : exp2f((wz[z] - mx) * 1.4426950408889634f);
-          tot += wz[z];
+#pragma unroll
+        for (int z = 0; z < kMaxSplits; ++z) {
+          if (z < prm.nsplit) {
+            wz[z] = (mx == -INFINITY || wz[z] == -INFINITY) ? 0.f : exp2f((wz[z] - mx) * 1.4426950408889634f);
+            tot += wz[z];
+          }
         }
         const float inv = tot > 0.f ? 1.f / tot : 0.f;
         for (int c = 0; c < kDvHalf; c += 8) {
