@@ -708,27 +708,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
     const size_t orow = ((size_t)t * prm.H + h) * kDv + half * kDvHalf;
     const float lse_v = l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+    const bool have_o = n > 0 && ok;
+    // O is read back from TMEM 64 columns at a time (one wait per two loads)
+    auto load_o64 = [&](int c0, uint32_t (&oa)[32], uint32_t (&ob)[32]) {
+      if (have_o) {
+        tmem_ld32(tmem + lane_base + kColO + c0, oa);
+        tmem_ld32(tmem + lane_base + kColO + c0 + 32, ob);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) oa[j] = ob[j] = 0u;
+      }
+    };
+    auto store_bf16_32 = [&](uint16_t* dst, const uint32_t (&ov)[32], float scale) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(ov[j]) * scale, __uint_as_float(ov[j + 1]) * scale);
+        pk[j >> 1] = *reinterpret_cast<uint32_t*>(&b2);
+      }
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+    };
     if (prm.nsplit == 1) {
-      for (int c = 0; c < kDvHalf / 32; ++c) {
-        uint32_t ov[32];
-        if (n > 0 && ok) {
-          tmem_ld32(tmem + lane_base + kColO + c * 32, ov);
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) ov[j] = 0u;
-        }
+#pragma unroll 1
+      for (int c0 = 0; c0 < kDvHalf; c0 += 64) {
+        uint32_t oa[32], ob[32];
+        load_o64(c0, oa, ob);
         if (hv) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            __nv_bfloat162 b2 =
-                __floats2bfloat162_rn(__uint_as_float(ov[j]) * inv_l, __uint_as_float(ov[j + 1]) * inv_l);
-            pk[j >> 1] = *reinterpret_cast<uint32_t*>(&b2);
-          }
-          uint4* dst = reinterpret_cast<uint4*>(prm.o + orow + c * 32);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          store_bf16_32(prm.o + orow + c0, oa, inv_l);
+          store_bf16_32(prm.o + orow + c0 + 32, ob, inv_l);
         }
       }
       if (hv && half == 0 && prm.lse) prm.lse[(size_t)t * prm.H + h] = lse_v;
@@ -736,21 +746,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       // split keys: write this split's normalised partial; the last CTA of the
       // (token, value half) group merges all splits and writes the output.
       float* op = prm.o_part + ((size_t)split * prm.T * prm.H) * kDv;
-      for (int c = 0; c < kDvHalf / 32; ++c) {
-        uint32_t ov[32];
-        if (n > 0 && ok) {
-          tmem_ld32(tmem + lane_base + kColO + c * 32, ov);
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) ov[j] = 0u;
-        }
+#pragma unroll 1
+      for (int c0 = 0; c0 < kDvHalf; c0 += 64) {
+        uint32_t oa[32], ob[32];
+        load_o64(c0, oa, ob);
         if (hv) {
-          float4* dst = reinterpret_cast<float4*>(op + orow + c * 32);
+          float4* dst = reinterpret_cast<float4*>(op + orow + c0);
 #pragma unroll
           for (int v = 0; v < 8; ++v)
-            dst[v] = make_float4(__uint_as_float(ov[4 * v]) * inv_l, __uint_as_float(ov[4 * v + 1]) * inv_l,
-                                 __uint_as_float(ov[4 * v + 2]) * inv_l, __uint_as_float(ov[4 * v + 3]) * inv_l);
+            dst[v] = make_float4(__uint_as_float(oa[4 * v]) * inv_l, __uint_as_float(oa[4 * v + 1]) * inv_l,
+                                 __uint_as_float(oa[4 * v + 2]) * inv_l, __uint_as_float(oa[4 * v + 3]) * inv_l);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[8 + v] = make_float4(__uint_as_float(ob[4 * v]) * inv_l, __uint_as_float(ob[4 * v + 1]) * inv_l,
+                                     __uint_as_float(ob[4 * v + 2]) * inv_l, __uint_as_float(ob[4 * v + 3]) * inv_l);
         }
       }
       // lse of this split as seen by this CTA (both value halves compute the
@@ -768,15 +777,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         *s_last = last;
       }
       named_bar_sync(2, 128);
-      if (*s_last && hv) {
+      if (*s_last) {  // uniform over the CTA: the TMEM reads below are warp-wide
         __threadfence();
         float wz[kMaxSplits];
         float mx = -INFINITY;
 #pragma unroll
         for (int z = 0; z < kMaxSplits; ++z) {
           if (z >= prm.nsplit) break;
-          wz[z] = __ldcg(prm.lse_part + (size_t)gridDim.x * 128 +
-                         (((size_t)z * prm.T + t) * gridDim.x + blockIdx.x) * 128 + r);
+          wz[z] = __ldcg(lsep + (((size_t)z * prm.T + t) * gridDim.x + blockIdx.x) * 128 + r);
           mx = fmaxf(mx, wz[z]);
         }
         float tot = 0.f;
@@ -788,38 +796,51 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const float inv = tot > 0.f ? 1.f / tot : 0.f;
-        for (int c = 0; c < kDvHalf; c += 8) {
-          float4 v0[kMaxSplits], v1[kMaxSplits];
+        // this CTA's own split comes from TMEM; the others from the
+        // partials, 32 columns (eight 16-byte loads in flight) at a time
+        float w_own = 0.f;
 #pragma unroll
-          for (int z = 0; z < kMaxSplits; ++z) {
-            if (z < prm.nsplit) {
-              const float* src = prm.o_part + ((size_t)z * prm.T * prm.H) * kDv + orow + c;
-              v0[z] = __ldcg(reinterpret_cast<const float4*>(src));
-              v1[z] = __ldcg(reinterpret_cast<const float4*>(src + 4));
+        for (int z = 0; z < kMaxSplits; ++z)
+          if (z == split) w_own = wz[z] * inv * inv_l;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kDvHalf; c0 += 64) {
+          uint32_t oa[32], ob[32];
+          load_o64(c0, oa, ob);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            oa[j] = __float_as_uint(__uint_as_float(oa[j]) * w_own);
+            ob[j] = __float_as_uint(__uint_as_float(ob[j]) * w_own);
+          }
+#pragma unroll 1
+          for (int z = 0; z < prm.nsplit; ++z) {
+            if (z == split) continue;
+            float wgt = 0.f;
+#pragma unroll
+            for (int q = 0; q < kMaxSplits; ++q)
+              if (q == z) wgt = wz[q] * inv;
+            const float4* src =
+                reinterpret_cast<const float4*>(prm.o_part + ((size_t)z * prm.T * prm.H) * kDv + orow + c0);
+            float4 v[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) v[u] = hv ? __ldcg(src + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              oa[4 * u] = __float_as_uint(fmaf(wgt, v[u].x, __uint_as_float(oa[4 * u])));
+              oa[4 * u + 1] = __float_as_uint(fmaf(wgt, v[u].y, __uint_as_float(oa[4 * u + 1])));
+              oa[4 * u + 2] = __float_as_uint(fmaf(wgt, v[u].z, __uint_as_float(oa[4 * u + 2])));
+              oa[4 * u + 3] = __float_as_uint(fmaf(wgt, v[u].w, __uint_as_float(oa[4 * u + 3])));
+              ob[4 * u] = __float_as_uint(fmaf(wgt, v[8 + u].x, __uint_as_float(ob[4 * u])));
+              ob[4 * u + 1] = __float_as_uint(fmaf(wgt, v[8 + u].y, __uint_as_float(ob[4 * u + 1])));
+              ob[4 * u + 2] = __float_as_uint(fmaf(wgt, v[8 + u].z, __uint_as_float(ob[4 * u + 2])));
+              ob[4 * u + 3] = __float_as_uint(fmaf(wgt, v[8 + u].w, __uint_as_float(ob[4 * u + 3])));
             }
           }
-          float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int z = 0; z < kMaxSplits; ++z) {
-            if (z < prm.nsplit) {
-              const float wgt = wz[z] * inv;
-              a[0] = fmaf(wgt, v0[z].x, a[0]);
-              a[1] = fmaf(wgt, v0[z].y, a[1]);
-              a[2] = fmaf(wgt, v0[z].z, a[2]);
-              a[3] = fmaf(wgt, v0[z].w, a[3]);
-              a[4] = fmaf(wgt, v1[z].x, a[4]);
-              a[5] = fmaf(wgt, v1[z].y, a[5]);
-              a[6] = fmaf(wgt, v1[z].z, a[6]);
-              a[7] = fmaf(wgt, v1[z].w, a[7]);
-            }
+          if (hv) {
+            store_bf16_32(prm.o + orow + c0, oa, 1.f);
+            store_bf16_32(prm.o + orow + c0 + 32, ob, 1.f);
           }
-          __nv_bfloat162 b0 = __floats2bfloat162_rn(a[0], a[1]), b1 = __floats2bfloat162_rn(a[2], a[3]);
-          __nv_bfloat162 b2 = __floats2bfloat162_rn(a[4], a[5]), b3 = __floats2bfloat162_rn(a[6], a[7]);
-          *reinterpret_cast<uint4*>(prm.o + orow + c) =
-              make_uint4(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1),
-                         *reinterpret_cast<uint32_t*>(&b2), *reinterpret_cast<uint32_t*>(&b3));
         }
-        if (half == 0 && prm.lse) prm.lse[(size_t)t * prm.H + h] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+        if (hv && half == 0 && prm.lse) prm.lse[(size_t)t * prm.H + h] = tot > 0.f ? mx + logf(tot) : -INFINITY;
       }
     }
   }
