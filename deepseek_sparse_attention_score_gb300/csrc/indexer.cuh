@@ -6,7 +6,7 @@
 
 namespace dsa {
 
-constexpr int kChunkDecode = 1024;   // keys per work item of one-token tiles
+constexpr int kChunkDecode = 512;    // keys per work item of one-token tiles
 constexpr int kChunkPrefill = 2048;  // keys per work item of 8-token tiles
 
 struct IndexerMeta {

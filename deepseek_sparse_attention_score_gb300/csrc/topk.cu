@@ -48,15 +48,13 @@ __device__ __forceinline__ int block_scan_warps(int v, int* s_tmp, int* total) {
   return r;
 }
 
-// Warp-aggregated histogram update: scores cluster in a few digits (the top
-// digit is the sign and high exponent bits), so lanes that share a digit add
-// once. All lanes of the warp must call it.
+// Histogram update into the calling warp's own 256-bin histogram. All lanes
+// of the warp must call it (it used to aggregate equal digits with a warp
+// match; a plain shared-memory atomic is cheaper for the digit spreads that
+// score rows have).
 __device__ __forceinline__ void hist_add(uint32_t* wh, uint32_t key, bool valid, uint32_t prefix, uint32_t mask,
                                          int shift) {
-  const bool act = valid && (key & mask) == prefix;
-  const uint32_t bin = act ? ((key >> shift) & 255u) : 256u;
-  const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-  if (act && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(wh + bin, (uint32_t)__popc(peers));
+  if (valid && (key & mask) == prefix) atomicAdd(wh + ((key >> shift) & 255u), 1u);
 }
 
 // Pick the digit holding the rank-`remaining` key from the 256-bin histogram
