@@ -56,7 +56,7 @@ constexpr int OFF_RINFO = OFF_RING + kRing * 32 * 4;         // uint32 mask[kRin
 constexpr int OFF_RBASE = OFF_RINFO + kRing * 8;             // int32 base row of contiguous steps [kRing]
 constexpr int OFF_SINFO = OFF_RBASE + kRing * 4;  // uint32 kend[kKStages], vmask[kVStages][2], vend[kVStages]
 constexpr int OFF_BAR = (OFF_SINFO + (kKStages + 3 * kVStages) * 4 + 7) & ~7;
-constexpr int NBAR = 2 * kKStages + 2 * kVStages + 2 * kRing + 6;
+constexpr int NBAR = 2 * kKStages + 2 * kVStages + 2 * kRing + 7;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int kSmem = OFF_MISC + 16;
 static_assert(kSmem <= 227 * 1024, "shared memory budget");
@@ -326,7 +326,8 @@ __device__ __forceinline__ void mma_issuer(uint32_t tmem, uint32_t qs_addr, uint
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_mla_kernel(const AttendParams prm, const __grid_constant__ CUtensorMap kvmap) {
+    sparse_mla_kernel(const AttendParams prm, const __grid_constant__ CUtensorMap kvmap,
+                      const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {
     if (threadIdx.x == 0) set_status(prm.dev_status, DSA_STATUS_INTERNAL);
@@ -357,6 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* pfull = sfull + 2;            // [2] 128 softmax threads (P written over S)
   uint64_t* pempty = sfull + 4;           // PV commit
   uint64_t* fin = sfull + 5;
+  uint64_t* qbar = sfull + 6;             // the query block's TMA copy
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
@@ -379,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(pfull + 1, 128);
     mbar_init(pempty, 1);
     mbar_init(fin, 1);
+    mbar_init(qbar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -386,16 +389,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  const int nh = min(128, prm.H - h0);
-  const uint16_t* qt = prm.q + ((size_t)t * prm.H + h0) * kDk;
-  // Q[:, 256:576] -> five 128-byte-swizzled column blocks in shared memory;
-  // Q[:, 0:256] staged row-major (528-byte rows, conflict-free 16-byte reads)
-  // in the still unused key stages, then moved into TMEM by the softmax warps.
-  constexpr int kQRowStage = kQTmemDims * 2 + 16;
-  static_assert(128 * kQRowStage <= kKStages * kKStageBytes + kVStages * kVStageBytes, "Q staging fits");
+  // barrier initialisation must be visible before the Q copy signals one
+  __syncthreads();
+  // Q rows h0..h0+127 of token t (rows past H belong to the next token or
+  // lie past the tensor, where TMA fills zeros; their outputs are never
+  // stored) as nine 128-byte-swizzled column blocks: Q[:, 256:576] stays in
+  // shared memory, Q[:, 0:256] waits in the still unused key stages until
+  // the softmax warps move it into TMEM.
   uint8_t* qstage = kst_s;
+  static_assert(kQTmemBlocks * 16384 <= kKStages * kKStageBytes, "Q staging fits");
+  if (tid == 0) {
+    mbar_arrive_expect_tx(qbar, (kDk / 64) * 16384);
+#pragma unroll 1
+    for (int c = 0; c < kDk / 64; ++c)
+      tma_load_2d(c < kQTmemBlocks ? qstage + c * 16384 : qs_s + (c - kQTmemBlocks) * 16384, &qmap, qbar, c * 64,
+                  t * prm.H + h0);
+  }
   // The key generator (warp 1) resolves its first window of selections while
-  // the other warps stage Q; it publishes steps only after the barrier below.
+  // Q arrives; it publishes steps only after the barrier below.
   TileGen gen;
   bool gen_more = false;
   long long gen_row = -1, gen_base = -1;
@@ -403,22 +414,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     gen.init(prm, t, split);
     gen_more = gen.next(gen_row, gen_mask, gen_base);
-  } else {
-    const uint32_t qbase = smem_u32(qs_s), stage = smem_u32(qstage);
-    constexpr int CH = kDk / 8;  // 72 chunks of 16 bytes per row
-    const int qtid = tid < 32 ? tid : tid - 32;  // warp 1 is busy generating keys
-    for (int c = qtid; c < 128 * CH; c += kThreads - 32) {
-      const int r = c / CH, ch = c % CH;
-      const bool ok = r < nh;
-      const uint16_t* src = ok ? qt + (size_t)r * kDk + ch * 8 : prm.q;
-      const uint32_t dst = ch < kQTmemDims / 8
-                               ? stage + r * kQRowStage + ch * 16
-                               : qbase + ((ch - kQTmemDims / 8) >> 3) * 16384 + sw128_offset(r, ch & 7);
-      cp_async16(dst, src, ok ? 16u : 0u);
-    }
-    cp_async_commit();
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
@@ -427,19 +422,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= 4 && warp < 8) {
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint4* src = reinterpret_cast<const uint4*>(qstage + r * kQRowStage);
+    if (mbar_wait(qbar, 0, abort_flag)) {
 #pragma unroll 1
-    for (int c0 = 0; c0 < kQTmemDims / 2; c0 += 32) {
-      uint32_t v[32];
+      for (int c = 0; c < kQTmemBlocks; ++c) {
+        const uint8_t* row = qstage + c * 16384 + r * 128;
+        uint32_t v[32];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint4 x = src[c0 / 4 + j];
-        v[4 * j] = x.x;
-        v[4 * j + 1] = x.y;
-        v[4 * j + 2] = x.z;
-        v[4 * j + 3] = x.w;
+        for (int j = 0; j < 8; ++j) {
+          const uint4 x = *reinterpret_cast<const uint4*>(row + ((j ^ (r & 7)) << 4));
+          v[4 * j] = x.x;
+          v[4 * j + 1] = x.y;
+          v[4 * j + 2] = x.z;
+          v[4 * j + 3] = x.w;
+        }
+        tmem_st32(tmem + lane_base + kColQ + c * 32, v);
       }
-      tmem_st32(tmem + lane_base + kColQ + c0, v);
     }
     tmem_st_wait();
   }
@@ -451,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const MmaBars br{kfull, kempty, vfull, vempty, sfull, pfull, pempty, fin};
+      mbar_wait(qbar, 0, abort_flag);
       if (half == 0)
         mma_issuer<0>(tmem, smem_u32(qs_s), smem_u32(kst_s), smem_u32(vst_s), br, kst_end, abort_flag);
       else
@@ -847,7 +845,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
-    if (*abort_flag && lane == 0) set_status(prm.dev_status, DSA_STATUS_TIMEOUT);
+    if (*abort_flag && lane == 0) {
+      set_status(prm.dev_status, DSA_STATUS_TIMEOUT);
+      mbar_wait_drain(qbar, 0);  // the Q copy must not land after the CTA exits
+    }
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -890,12 +891,13 @@ int run_attend(cudaStream_t stream, AttendParams prm, void* ws, size_t ws_bytes)
                                           lse_bytes(prm.T, prm.H, prm.nsplit));
     if (cudaMemsetAsync(prm.counters, 0, (size_t)prm.T * cols * 4, stream) != cudaSuccess) return DSA_ERR_CUDA;
   }
-  CUtensorMap kvmap;
+  CUtensorMap kvmap, qmap;
   if (!encode_bf16_2d(&kvmap, prm.kv, (uint64_t)prm.P * prm.ps, (uint64_t)prm.row_stride, 32, kDk))
     return DSA_ERR_CUDA;
+  if (!encode_bf16_2d(&qmap, prm.q, (uint64_t)prm.T * prm.H, kDk, 128, kDk)) return DSA_ERR_CUDA;
   set_smem_attr_once(reinterpret_cast<const void*>(sparse_mla_kernel), kSmem);
   dim3 grid(cols, prm.T, prm.nsplit);
-  sparse_mla_kernel<<<grid, kThreads, kSmem, stream>>>(prm, kvmap);
+  sparse_mla_kernel<<<grid, kThreads, kSmem, stream>>>(prm, kvmap, qmap);
   DSA_CHECK_LAUNCH();
   return DSA_OK;
 }

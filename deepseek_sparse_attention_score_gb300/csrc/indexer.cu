@@ -44,12 +44,30 @@ __device__ int block_excl_scan(int v, int* s_warp, int* total) {
   return excl;
 }
 
+constexpr int kPlanStageS = 4096;  // requests whose query offsets the planner keeps in shared memory
+
 __global__ void __launch_bounds__(1024) indexer_plan_kernel(IndexerMeta m, IndexerPlan pl, int ch1, int ch8) {
   __shared__ int s_warp[32];
+  __shared__ int s_cuq[kPlanStageS + 1];
   const int T = m.T, S = m.S, ps = m.ps;
+  // token -> request searches run against a shared-memory copy of cu_q_lens
+  // when it fits (a chain of dependent global loads otherwise)
+  const bool staged = S <= kPlanStageS;
+  if (staged)
+    for (int i = threadIdx.x; i <= S; i += blockDim.x) s_cuq[i] = __ldg(m.cu_q_lens + i);
+  __syncthreads();
+  auto seq_of = [&](int t) -> int {
+    if (!staged) return seq_of_token(m.cu_q_lens, S, t);
+    int lo = 0, hi = S - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_cuq[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+  };
   // 1. visible prefix of every token, clamped to the request's page-table span
   for (int t = threadIdx.x; t < T; t += blockDim.x) {
-    TokenGeom g = token_geom(m.seq_lens, m.cu_q_lens, m.cu_kv_lens, S, ps, m.max_kv, t, m.dev_status);
+    TokenGeom g = token_geom(m.seq_lens, m.cu_q_lens, m.cu_kv_lens, S, ps, m.max_kv, t, m.dev_status, seq_of(t));
     long long cap = (long long)(m.PTW - g.page_base) * ps;
     int nv = g.n_vis;
     if (g.page_base < 0 || (long long)nv > cap) {
@@ -68,7 +86,7 @@ __global__ void __launch_bounds__(1024) indexer_plan_kernel(IndexerMeta m, Index
     const int s = s0 + threadIdx.x;
     int nd = 0, np = 0;
     if (s < S) {
-      const int ql = __ldg(m.cu_q_lens + s + 1) - __ldg(m.cu_q_lens + s);
+      const int ql = staged ? s_cuq[s + 1] - s_cuq[s] : __ldg(m.cu_q_lens + s + 1) - __ldg(m.cu_q_lens + s);
       if (ql > 0) {
         const int nt = (ql + 7) / 8;
         nd = (ql - 8 * (nt - 1)) == 1 ? 1 : 0;
@@ -86,8 +104,9 @@ __global__ void __launch_bounds__(1024) indexer_plan_kernel(IndexerMeta m, Index
   const int n_dec_tiles = carry_d, n_pre_tiles = carry_p;
   // 3. tile descriptors {first token, ntok, request, visible keys of the last token}
   for (int t = threadIdx.x; t < T; t += blockDim.x) {
-    const int s = seq_of_token(m.cu_q_lens, S, t);
-    const int q0 = __ldg(m.cu_q_lens + s), ql = __ldg(m.cu_q_lens + s + 1) - q0;
+    const int s = seq_of(t);
+    const int q0 = staged ? s_cuq[s] : __ldg(m.cu_q_lens + s);
+    const int ql = (staged ? s_cuq[s + 1] : __ldg(m.cu_q_lens + s + 1)) - q0;
     const int r = t - q0;
     if (r % 8) continue;
     const int ntok = min(8, ql - r);
