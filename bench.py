@@ -176,7 +176,9 @@ def stage_roofline(wl, rn, timed):
     decode indexer 256 B per visible key and decode attention 1152 B per
     selected visible key (HBM); prefill indexer 2*32*128 FLOP per visible
     (query, key) pair and query-block attention 2*H*(576+512) FLOP per
-    (query, selected visible key) pair (tensor, bf16)."""
+    (query, selected visible key) pair (tensor, bf16). The paged write-back
+    that precedes the path is timed beside them (not part of the step):
+    2 B read + 2 B written per copied element (HBM)."""
     import numpy as np
     import torch
 
@@ -210,6 +212,23 @@ def stage_roofline(wl, rn, timed):
         name = "indexer_page_topk" if rn.page_budget is not None else "indexer_topk"
         out[name] = entry(timed(lambda: rn.index(0)), 256 * nvis.sum(), "hbm")
         out["sparse_mla_decode"] = entry(timed(lambda: rn.attend(0)), 1152 * keys, "hbm")
+    # the step before the path: paged write-back of every query token's
+    # latent row and indexer key (the rows already there are written back
+    # unchanged, so the caches keep their contents): 2 x (576 + 128) x 2 B per
+    # token, read and written
+    import deepseek_sparse_attention_score_gb300 as dsa
+
+    tseq, tpos = rg.token_seq(), rg.token_pos()
+    ent = rg.cu_kv_lens[tseq] // ps + tpos // ps
+    phys = torch.from_numpy((rg.page_indices[ent].astype(np.int64) * ps + tpos % ps)).to(rn.kv[0].device)
+    kv_rows = rn.kv[0].view(-1, rn.kv[0].shape[-1]).index_select(0, phys)[:, :576].contiguous()
+    k_rows = rn.kcache[0].view(-1, 128).index_select(0, phys).contiguous()
+
+    def write_back():
+        dsa.dsa_paged_write_back(kv_rows, rn.kv[0], *rn.meta, D=576, dev_status=rn.status)
+        dsa.dsa_paged_write_back(k_rows, rn.kcache[0], *rn.meta, D=128, dev_status=rn.status)
+
+    out["paged_write_back"] = entry(timed(write_back), 2 * (576 + 128) * 2 * rg.T, "hbm")
     return out
 
 

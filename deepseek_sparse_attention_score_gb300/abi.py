@@ -41,6 +41,7 @@ EXPORTS = (
     "dsa_sparse_mla_decode_workspace_size",
     "dsa_sparse_mla_decode",
     "dsa_sparse_mla_prefill_qblock",
+    "dsa_paged_write_back",
     "dsa_device_sm_count",
     "dsa_launch_count",
     "dsa_sparse_mla_decode_noalloc",
@@ -86,6 +87,7 @@ def lib() -> ctypes.CDLL:
                                                 _I, _I, _I, _I, _F, _P, _P, _P]
     L.dsa_sparse_mla_decode_noalloc.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                                 _I, _I, _F, _P, _P, _P]
+    L.dsa_paged_write_back.argtypes = [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]
     L.dsa_device_sm_count.argtypes = []
     L.dsa_launch_count.argtypes = []
     L.dsa_launch_count.restype = ctypes.c_longlong
@@ -329,3 +331,22 @@ def dsa_sparse_mla_decode_noalloc(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_i
                                              _ptr(dev_status))
     _check("dsa_sparse_mla_decode_noalloc", rc)
     return (o, lse) if lse is not None else o
+
+
+# ------------------------------------------------------------ write-back
+def dsa_paged_write_back(rows, cache, seq_lens, cu_q_lens, cu_kv_lens, page_indices, *, D=None, dev_status=None):
+    """Write each query token's row (``rows`` [T, W], its first ``D`` columns)
+    into its slot of the paged ``cache`` [P, ps, W'] in place."""
+    dev = cache.device
+    _need(rows, "rows", torch.bfloat16, dev, 2)
+    _need(cache, "cache", torch.bfloat16, dev, 3)
+    S, PTW = _meta(dev, seq_lens, cu_q_lens, cu_kv_lens, page_indices)
+    T, src_stride = rows.shape
+    P, ps, cache_stride = cache.shape
+    if D is None:
+        D = min(src_stride, cache_stride)
+    rc = lib().dsa_paged_write_back(_stream(dev), _ptr(rows), src_stride, D, _ptr(cache), cache_stride,
+                                    _ptr(seq_lens), _ptr(cu_q_lens), _ptr(cu_kv_lens), _ptr(page_indices), T, S, P,
+                                    PTW, ps, _ptr(dev_status))
+    _check("dsa_paged_write_back", rc)
+    return cache

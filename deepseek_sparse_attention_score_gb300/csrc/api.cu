@@ -135,6 +135,20 @@ using namespace dsa;
 extern "C" {
 
 int dsa_device_sm_count(void) { return sm_count(); }
+
+int dsa_paged_write_back(dsa_stream_t stream, const uint16_t* rows, int src_stride, int D, uint16_t* cache,
+                         int cache_stride, const int32_t* seq_lens, const int32_t* cu_q_lens,
+                         const int32_t* cu_kv_lens, const int32_t* page_indices, int T, int S, int P, int PTW,
+                         int ps, int32_t* dev_status) {
+  if (T < 0 || S < 0 || P < 0 || PTW < 0 || D < 0) return DSA_ERR_INVALID_ARGUMENT;
+  if (T == 0 || D == 0) return DSA_OK;
+  if (S < 1 || P < 1 || PTW < 1 || ps < 1) return DSA_ERR_INVALID_ARGUMENT;
+  if (!rows || !cache || !seq_lens || !cu_q_lens || !cu_kv_lens || !page_indices) return DSA_ERR_INVALID_ARGUMENT;
+  if (D % 8 || src_stride % 8 || cache_stride % 8 || D > src_stride || D > cache_stride) return DSA_ERR_UNSUPPORTED;
+  if (!aligned16(rows) || !aligned16(cache)) return DSA_ERR_ALIGNMENT;
+  return run_paged_write_back(static_cast<cudaStream_t>(stream), rows, src_stride, D, cache, cache_stride, seq_lens,
+                              cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps, dev_status);
+}
 long long dsa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int dsa_index_build_share_map(const int32_t* types, int num_layers, int skip_offset, int32_t* full_slot,

@@ -44,4 +44,10 @@ int run_block_union(cudaStream_t stream, const int32_t* topk_units, int T, int K
                     const int32_t* cu_q_lens, const int32_t* cu_kv_lens, int S, int ps, int PTW, int32_t* units,
                     uint32_t* member, int32_t* counts, int32_t* dev_status);
 
+// Paged write-back of new token rows (writeback.cu).
+int run_paged_write_back(cudaStream_t stream, const uint16_t* rows, long long src_stride, int D, uint16_t* cache,
+                         long long cache_stride, const int32_t* seq_lens, const int32_t* cu_q_lens,
+                         const int32_t* cu_kv_lens, const int32_t* page_indices, int T, int S, int P, int PTW,
+                         int ps, int32_t* dev_status);
+
 }  // namespace dsa

@@ -228,6 +228,33 @@ DSA_API int dsa_sparse_mla_prefill_qblock(dsa_stream_t stream, const uint16_t* q
                                   int H, int Dk, int Dv, float sm_scale, uint16_t* o, float* lse,
                                   int32_t* dev_status);
 
+/* ------------------------------------------------------------------------
+ * Paged write-back of the new tokens' rows into a paged cache: the step
+ * directly before the indexer and the attention, which read these rows.
+ * dsa_sparse_backend.py, _scatter_paged (and the Pallas paged_write_back of
+ * sparse_mla_prefill_qblock.py): query token t of request s sits at position
+ * pos(t) = seq_lens[s] - q_len(s) + (t - cu_q_lens[s]) and its row is copied
+ * to row pos(t) % ps of physical page page_indices[cu_kv_lens[s]/ps +
+ * pos(t)/ps]. Every other cache row is left untouched.
+ *   rows   bf16 [T, src_stride]  the first D columns of row t are written
+ *   cache  bf16 [P, ps, cache_stride]  updated in place; the first D columns
+ *          of the destination rows are overwritten
+ * Use it once per cache: D = 576 for the latent [c_kv | k_rope] cache
+ * (cache_stride 576 or 640), D = 128 for the indexer key cache.
+ * There are no padding rows in this ABI (T == cu_q_lens[S]), so no row is
+ * sent to a sentinel page: a token whose destination falls outside the page
+ * table or the pool sets DSA_STATUS_BAD_METADATA and is skipped.
+ * Supported: D, src_stride, cache_stride multiples of 8 (16-byte rows),
+ * D <= src_stride, D <= cache_stride, rows and cache 16-byte aligned.
+ * Needs no workspace. Tokens write distinct rows whenever the metadata is
+ * valid (positions of one request are distinct, requests own disjoint
+ * page-table entries that map to distinct pages).
+ * ------------------------------------------------------------------------ */
+DSA_API int dsa_paged_write_back(dsa_stream_t stream, const uint16_t* rows, int src_stride, int D, uint16_t* cache,
+                                 int cache_stride, const int32_t* seq_lens, const int32_t* cu_q_lens,
+                                 const int32_t* cu_kv_lens, const int32_t* page_indices, int T, int S, int P,
+                                 int PTW, int ps, int32_t* dev_status);
+
 /* Number of streaming multiprocessors the kernels size their grids for
  * (device of the current context); a query helper, no device work. */
 DSA_API int dsa_device_sm_count(void);

@@ -9,7 +9,8 @@ path, written from the sglang-jax DSA pages:
     ``build_block_unit_tables``, ``_qblock_kernel``,
     ``sparse_mla_attention_qblock``, ``prefill_write_and_attend_ragged_qblock``;
   * "dsa_sparse_backend.py" (DSA sparse attention backend): the IndexShare
-    dispatch and the page budget of the prefill page top-k.
+    dispatch, the page budget of the prefill page top-k, and the paged cache
+    write of the new tokens (``_scatter_paged``) that precedes the path.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
 leg may import this module. It shares no code with the CUDA library and
@@ -387,3 +388,28 @@ def dense_mla(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, sm_scale, Dv
         wgt = np.exp(logit - mx)
         out.append((wgt.T @ vals) / wgt.sum(axis=0)[:, None])
     return np.stack(out)
+
+
+# ---------------------------------------------------------------------------
+# the step before the path: paged write-back of the new tokens' rows
+# ---------------------------------------------------------------------------
+
+def paged_write_back(cache, rows, seq_lens, cu_q_lens, cu_kv_lens, page_indices):
+    """Copy of ``cache`` [P, ps, W] with every query token's row written at its
+    own slot (dsa_sparse_backend.py, ``_scatter_paged``): token t of request s
+    lands at absolute position ``pos = kv_len - q_len + (t - q_start)``, i.e.
+    row ``pos % ps`` of physical page ``page_indices[cu_kv_lens[s]//ps +
+    pos//ps]``; the first ``rows.shape[1]`` columns are overwritten. The
+    pages' padding rows (sent to a sentinel page) do not occur here: every
+    token belongs to a request."""
+    out = np.array(cache, copy=True)
+    ps = out.shape[1]
+    D = np.asarray(rows).shape[1]
+    cu = np.asarray(cu_q_lens, dtype=np.int64)
+    seq = token_seq(cu)
+    pos = token_pos(seq_lens, cu)
+    for t in range(int(cu[-1])):
+        s = int(seq[t])
+        entry = int(cu_kv_lens[s]) // ps + int(pos[t]) // ps
+        out[int(page_indices[entry]), int(pos[t]) % ps, :D] = rows[t][:D]
+    return out

@@ -373,3 +373,50 @@ def test_widen_bf16_bits_exact():
     vals = O.widen(bits)
     assert vals[0] == 1.0 and vals[1] == -1.0 and vals[3] == 0.0 and np.isinf(vals[5])
     assert vals[2] == 3.140625
+
+
+# ------------------------------------------------ paged write-back (before a1)
+def test_write_back_hand_example():
+    # one request, page size 4, pages [2, 0, 1]: kv_len 6 with 2 new tokens at
+    # positions 4 and 5 -> logical page 1 -> physical page 0, rows 0 and 1
+    cache = np.zeros((3, 4, 2), np.float32)
+    rows = np.array([[1.0, 2.0], [3.0, 4.0]])
+    out = O.paged_write_back(cache, rows, seq_lens=[6], cu_q_lens=[0, 2], cu_kv_lens=[0, 12],
+                             page_indices=[2, 0, 1])
+    expect = np.zeros_like(cache)
+    expect[0, 0] = [1.0, 2.0]
+    expect[0, 1] = [3.0, 4.0]
+    np.testing.assert_array_equal(out, expect)
+    assert cache.sum() == 0  # the input is not modified
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_write_back_round_trip_and_untouched_rows(seed):
+    # ragged batch (decode, extend, empty request, prefill): reading the written
+    # cache back through the independent position -> row map returns each
+    # token's row, at exactly its position, and leaves every other row as is
+    rng = np.random.default_rng(seed)
+    ps = 8
+    q_lens = np.array([1, 5, 0, 12])
+    kv_lens = np.array([19, 30, 3, 12])
+    npages = -(-kv_lens // ps)
+    cu_kv = np.concatenate([[0], np.cumsum(npages * ps)])
+    P = int(npages.sum()) + 2
+    page_indices = rng.permutation(P)[: int(npages.sum())]
+    cu_q = np.concatenate([[0], np.cumsum(q_lens)])
+    T, W, D = int(cu_q[-1]), 10, 7
+    cache = rng.standard_normal((P, ps, W))
+    rows = rng.standard_normal((T, D))
+    out = O.paged_write_back(cache, rows, kv_lens, cu_q, cu_kv, page_indices)
+    written = np.zeros((P * ps,), bool)
+    t = 0
+    for s in range(len(q_lens)):
+        for j in range(q_lens[s]):
+            pos = kv_lens[s] - q_lens[s] + j
+            r = int(O.physical_rows(cu_kv, page_indices, ps, s, [pos])[0])
+            np.testing.assert_array_equal(out.reshape(-1, W)[r, :D], rows[t])
+            np.testing.assert_array_equal(out.reshape(-1, W)[r, D:], cache.reshape(-1, W)[r, D:])
+            assert not written[r]
+            written[r] = True
+            t += 1
+    np.testing.assert_array_equal(out.reshape(-1, W)[~written], cache.reshape(-1, W)[~written])
