@@ -42,6 +42,7 @@ EXPORTS = (
     "dsa_sparse_mla_decode",
     "dsa_sparse_mla_prefill_qblock",
     "dsa_paged_write_back",
+    "dsa_topk_pages_from_tokens",
     "dsa_device_sm_count",
     "dsa_launch_count",
     "dsa_sparse_mla_decode_noalloc",
@@ -88,6 +89,7 @@ def lib() -> ctypes.CDLL:
     L.dsa_sparse_mla_decode_noalloc.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                                 _I, _I, _F, _P, _P, _P]
     L.dsa_paged_write_back.argtypes = [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]
+    L.dsa_topk_pages_from_tokens.argtypes = [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P]
     L.dsa_device_sm_count.argtypes = []
     L.dsa_launch_count.argtypes = []
     L.dsa_launch_count.restype = ctypes.c_longlong
@@ -350,3 +352,20 @@ def dsa_paged_write_back(rows, cache, seq_lens, cu_q_lens, cu_kv_lens, page_indi
                                     PTW, ps, _ptr(dev_status))
     _check("dsa_paged_write_back", rc)
     return cache
+
+
+def dsa_topk_pages_from_tokens(topk, *, ps, max_pages, cap=512, pages=None, counts=None, dev_status=None):
+    """Ascending unique pages of each query's selected tokens, the first
+    ``cap`` of them, -1 padded; returns ``(pages [T, cap], counts [T])`` with
+    the uncapped number of unique pages per row."""
+    dev = topk.device
+    _need(topk, "topk", torch.int32, dev, 2)
+    T, K = topk.shape
+    if pages is None:
+        pages = torch.empty((T, cap), dtype=torch.int32, device=dev)
+    if counts is None:
+        counts = torch.empty((T,), dtype=torch.int32, device=dev)
+    rc = lib().dsa_topk_pages_from_tokens(_stream(dev), _ptr(topk), T, K, ps, max_pages, cap, _ptr(pages),
+                                          _ptr(counts), _ptr(dev_status))
+    _check("dsa_topk_pages_from_tokens", rc)
+    return pages, counts

@@ -136,6 +136,16 @@ extern "C" {
 
 int dsa_device_sm_count(void) { return sm_count(); }
 
+int dsa_topk_pages_from_tokens(dsa_stream_t stream, const int32_t* topk, int T, int K, int ps, int max_pages,
+                               int cap, int32_t* pages, int32_t* counts, int32_t* dev_status) {
+  if (T < 0 || K < 0 || ps < 1 || cap < 1) return DSA_ERR_INVALID_ARGUMENT;
+  if (max_pages < 1 || max_pages > topk_pages_max_pages()) return DSA_ERR_UNSUPPORTED;
+  if (T == 0) return DSA_OK;
+  if (!pages || (K > 0 && !topk)) return DSA_ERR_INVALID_ARGUMENT;
+  return run_topk_pages(static_cast<cudaStream_t>(stream), topk, T, K, ps, max_pages, cap, pages, counts,
+                        dev_status);
+}
+
 int dsa_paged_write_back(dsa_stream_t stream, const uint16_t* rows, int src_stride, int D, uint16_t* cache,
                          int cache_stride, const int32_t* seq_lens, const int32_t* cu_q_lens,
                          const int32_t* cu_kv_lens, const int32_t* page_indices, int T, int S, int P, int PTW,

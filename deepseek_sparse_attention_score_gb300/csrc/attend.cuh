@@ -50,4 +50,9 @@ int run_paged_write_back(cudaStream_t stream, const uint16_t* rows, long long sr
                          const int32_t* cu_kv_lens, const int32_t* page_indices, int T, int S, int P, int PTW,
                          int ps, int32_t* dev_status);
 
+// Token top-k -> sorted unique page list per query (pages.cu).
+int topk_pages_max_pages();
+int run_topk_pages(cudaStream_t stream, const int32_t* topk, int T, int K, int ps, int max_pages, int cap,
+                   int32_t* pages, int32_t* counts, int32_t* dev_status);
+
 }  // namespace dsa

@@ -255,6 +255,22 @@ DSA_API int dsa_paged_write_back(dsa_stream_t stream, const uint16_t* rows, int 
                                  const int32_t* cu_kv_lens, const int32_t* page_indices, int T, int S, int P,
                                  int PTW, int ps, int32_t* dev_status);
 
+/* ------------------------------------------------------------------------
+ * Token top-k -> page list, for the page-level decode shape of the pages.
+ * dsa_sparse_backend.py, compute_topk_pages (k_pages_max = 512 there): per
+ * query row, the ascending unique pages (position / ps) of the selected
+ * tokens; the first `cap` of them are written, the rest of the row is -1.
+ *   topk   int32 [T, K]  token positions, any order, -1 entries ignored
+ *   pages  int32 [T, cap] out
+ *   counts int32 [T] out or NULL: number of unique pages (not capped), so
+ *          counts[t] > cap means row t was truncated
+ * A position at or beyond max_pages * ps sets DSA_STATUS_BAD_INDEX and is
+ * ignored. Supported: 1 <= max_pages <= 2^20, cap >= 1. Needs no workspace.
+ * ------------------------------------------------------------------------ */
+DSA_API int dsa_topk_pages_from_tokens(dsa_stream_t stream, const int32_t* topk, int T, int K, int ps,
+                                       int max_pages, int cap, int32_t* pages, int32_t* counts,
+                                       int32_t* dev_status);
+
 /* Number of streaming multiprocessors the kernels size their grids for
  * (device of the current context); a query helper, no device work. */
 DSA_API int dsa_device_sm_count(void);

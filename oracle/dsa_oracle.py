@@ -413,3 +413,17 @@ def paged_write_back(cache, rows, seq_lens, cu_q_lens, cu_kv_lens, page_indices)
         entry = int(cu_kv_lens[s]) // ps + int(pos[t]) // ps
         out[int(page_indices[entry]), int(pos[t]) % ps, :D] = rows[t][:D]
     return out
+
+
+def topk_pages_of_tokens(topk_row, ps, cap):
+    """Page list of one query's token selections (dsa_sparse_backend.py,
+    ``compute_topk_pages``, whose module the pages import but do not show;
+    the plain reading): the ascending unique pages ``position // ps`` of the
+    selected tokens, the first ``cap`` of them, -1 padded; also the uncapped
+    number of unique pages."""
+    row = np.asarray(topk_row, dtype=np.int64)
+    uniq = np.unique(row[row >= 0] // ps)
+    out = np.full(cap, -1, dtype=np.int64)
+    n = min(cap, len(uniq))
+    out[:n] = uniq[:n]
+    return out, len(uniq)

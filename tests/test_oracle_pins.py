@@ -420,3 +420,23 @@ def test_write_back_round_trip_and_untouched_rows(seed):
             written[r] = True
             t += 1
     np.testing.assert_array_equal(out.reshape(-1, W)[~written], cache.reshape(-1, W)[~written])
+
+
+# ---------------------------------------- token top-k -> page list (NEXT-2)
+def test_topk_pages_of_tokens_closed_forms():
+    pages, n = O.topk_pages_of_tokens([130, 5, -1, 64, 127, 0, 63], 64, 4)
+    assert pages.tolist() == [0, 1, 2, -1] and n == 3
+    pages, n = O.topk_pages_of_tokens([-1, -1], 64, 2)
+    assert pages.tolist() == [-1, -1] and n == 0
+    # truncation keeps the lowest pages; page size 1 turns it into a sort
+    pages, n = O.topk_pages_of_tokens([9, 3, 7, 3, 1], 1, 3)
+    assert pages.tolist() == [1, 3, 7] and n == 4
+
+
+def test_topk_pages_cover_exactly_the_selected_tokens():
+    rng = np.random.default_rng(5)
+    row = rng.choice(5000, size=700, replace=False)
+    pages, n = O.topk_pages_of_tokens(row, 64, 200)
+    got = set(pages[pages >= 0].tolist())
+    assert got == {int(j) // 64 for j in row} and n == len(got)
+    assert all(a < b for a, b in zip(pages[:n], pages[1:n]))
