@@ -42,6 +42,7 @@ EXPORTS = (
     "dsa_sparse_mla_decode",
     "dsa_sparse_mla_prefill_qblock",
     "dsa_paged_write_back",
+    "dsa_dense_mla",
     "dsa_topk_pages_from_tokens",
     "dsa_device_sm_count",
     "dsa_launch_count",
@@ -90,6 +91,8 @@ def lib() -> ctypes.CDLL:
                                                 _I, _I, _F, _P, _P, _P]
     L.dsa_paged_write_back.argtypes = [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]
     L.dsa_topk_pages_from_tokens.argtypes = [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P]
+    L.dsa_dense_mla.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _F,
+                                _P, _P, _P, _Z, _P]
     L.dsa_device_sm_count.argtypes = []
     L.dsa_launch_count.argtypes = []
     L.dsa_launch_count.restype = ctypes.c_longlong
@@ -369,3 +372,28 @@ def dsa_topk_pages_from_tokens(topk, *, ps, max_pages, cap=512, pages=None, coun
                                           _ptr(counts), _ptr(dev_status))
     _check("dsa_topk_pages_from_tokens", rc)
     return pages, counts
+
+
+def dsa_dense_mla(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, *, max_kv, sm_scale, sliding_window=0,
+                  soft_cap=0.0, o=None, lse=None, want_lse=False, ws=None, dev_status=None, Dv=512):
+    """Dense causal absorbed-MLA over every visible position (optionally the
+    ``sliding_window`` most recent ones, with a tanh logit cap)."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev, 3)
+    _need(kv, "kv", torch.bfloat16, dev, 3)
+    S, PTW = _meta(dev, seq_lens, cu_q_lens, cu_kv_lens, page_indices)
+    T, H, Dk = q.shape
+    P, ps, row_stride = kv.shape
+    if o is None:
+        o = torch.empty((T, H, Dv), dtype=torch.bfloat16, device=dev)
+    if want_lse and lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if ws is None:
+        nb = dsa_sparse_mla_decode_workspace_size(T, H, Dv)
+        ws = torch.empty(max(1, nb), dtype=torch.uint8, device=dev)
+    rc = lib().dsa_dense_mla(_stream(dev), _ptr(q), _ptr(kv), row_stride, _ptr(seq_lens), _ptr(cu_q_lens),
+                             _ptr(cu_kv_lens), _ptr(page_indices), int(max_kv), T, S, P, PTW, ps, H, Dk, Dv,
+                             float(sm_scale), int(sliding_window), float(soft_cap), _ptr(o), _ptr(lse), _ptr(ws),
+                             ws.numel(), _ptr(dev_status))
+    _check("dsa_dense_mla", rc)
+    return (o, lse) if lse is not None else o

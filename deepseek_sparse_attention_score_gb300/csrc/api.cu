@@ -271,6 +271,49 @@ int dsa_sparse_mla_decode(dsa_stream_t stream, const uint16_t* q, const uint16_t
 // No-allocation variant of dsa_sparse_mla_decode (declared in dsa.h): the
 // same checks and split choice; the split scratch is the library's built-in
 // device array instead of a caller workspace.
+int dsa_dense_mla(dsa_stream_t stream, const uint16_t* q, const uint16_t* kv, int row_stride, const int32_t* seq_lens,
+                  const int32_t* cu_q_lens, const int32_t* cu_kv_lens, const int32_t* page_indices, int max_kv,
+                  int T, int S, int P, int PTW, int ps, int H, int Dk, int Dv, float sm_scale, int sliding_window,
+                  float soft_cap, uint16_t* o, float* lse, void* ws, size_t ws_bytes, int32_t* dev_status) {
+  int rc = check_meta(seq_lens, cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps);
+  if (rc) return rc;
+  rc = attend_check(q, kv, row_stride, T, H, Dk, Dv, o);
+  if (rc) return rc;
+  if (max_kv < 1 || sliding_window < 0) return DSA_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(sm_scale) || !std::isfinite(soft_cap) || soft_cap < 0.f) return DSA_ERR_INVALID_ARGUMENT;
+  if (T == 0 || H == 0) return DSA_OK;
+  AttendParams prm{};
+  prm.q = q;
+  prm.kv = kv;
+  prm.row_stride = row_stride;
+  prm.seq_lens = seq_lens;
+  prm.cu_q_lens = cu_q_lens;
+  prm.cu_kv_lens = cu_kv_lens;
+  prm.page_indices = page_indices;
+  prm.T = T;
+  prm.S = S;
+  prm.P = P;
+  prm.PTW = PTW;
+  prm.ps = ps;
+  prm.H = H;
+  prm.scale_log2 = sm_scale * 1.4426950408889634f;
+  prm.mode = kModeDense;
+  prm.window = sliding_window;
+  if (soft_cap > 0.f) {
+    prm.soft_cap_on = 1;
+    prm.inv_cap_scale = sm_scale / soft_cap;
+    prm.cap_log2 = soft_cap * 1.4426950408889634f;
+  }
+  prm.K = (max_kv + ps - 1) / ps;  // pages of the longest request: the split unit
+  prm.o = o;
+  prm.lse = lse;
+  prm.dev_status = dev_status;
+  int z = attend_num_splits(T, H, prm.K, prm.mode);
+  if (z > 1 && (!ws || ws_bytes < attend_workspace_bytes(T, H, z) || !aligned16(ws))) z = 1;
+  prm.nsplit = z;
+  return run_attend(static_cast<cudaStream_t>(stream), prm, ws, ws_bytes);
+}
+
 int dsa_sparse_mla_decode_noalloc(dsa_stream_t stream, const uint16_t* q, const uint16_t* kv, int row_stride,
                                   const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
                                   const int32_t* page_indices, const int32_t* sel, int K, int unit, int T, int S,

@@ -96,6 +96,7 @@ struct TileGen {
   int w_phys;         // this lane's unit: physical page, -1 if none
   int cur_key0, cur_phys, sub, cur_valid;
   int b, qq, cnt;     // qblock
+  int key_lo;         // dense: first key position inside the window
 
   __device__ void init(const AttendParams& prm, int tok, int split) {
     p = &prm;
@@ -113,7 +114,17 @@ struct TileGen {
     pend = 0;
     sub = 0;
     cur_valid = 0;
-    if (mode == kModeQblock) {
+    key_lo = 0;
+    if (mode == kModeDense) {
+      // every page that holds a visible position inside the window, split
+      // evenly across the CTAs of this token
+      key_lo = prm.window > 0 ? max(0, pos - prm.window + 1) : 0;
+      const int p_lo = key_lo / prm.ps, p_hi = (n_vis + prm.ps - 1) / prm.ps;
+      const int per = (max(0, p_hi - p_lo) + prm.nsplit - 1) / prm.nsplit;
+      e = min(p_hi, p_lo + split * per);
+      e1 = min(p_hi, e + per);
+      win = e;
+    } else if (mode == kModeQblock) {
       b = tok / prm.QB;
       qq = tok % prm.QB;
       cnt = min(__ldg(prm.counts + b), prm.u_max);
@@ -191,6 +202,8 @@ struct TileGen {
         bool v;
         if (mode == kModePage) {
           v = cur_key0 + k0 < n_vis;
+        } else if (mode == kModeDense) {
+          v = cur_key0 + k0 < n_vis && cur_key0 + k0 >= key_lo;
         } else {
           const int kp = cur_key0 + k0;  // kp = g*ps + r - base_tok
           v = kp <= pos && kp < kv_len;
@@ -206,7 +219,12 @@ struct TileGen {
       sub = 0;
       if (!pend) {
         // resolve a window of 32 candidate units to physical pages
-        if (mode == kModePage) {
+        if (mode == kModeDense) {
+          if (win >= e1) return false;
+          const int pgl = win + lane;
+          w_phys = pgl < e1 ? page_of(page_base + pgl) : -1;
+          w_key0 = pgl * ps;
+        } else if (mode == kModePage) {
           if (win >= e1) return false;
           const int ee = win + lane;
           const int pgl = ee < e1 ? __ldg(p->sel + (size_t)t * p->K + ee) : -1;
@@ -325,6 +343,9 @@ __device__ __forceinline__ void mma_issuer(uint32_t tmem, uint32_t qs_addr, uint
   }
 }
 
+// kSoftCap: the logit cap of the dense fallback, a separate instantiation
+// so that the common path carries none of its code
+template <bool kSoftCap>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_mla_kernel(const AttendParams prm, const __grid_constant__ CUtensorMap kvmap,
                       const __grid_constant__ CUtensorMap qmap) {
@@ -483,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // decode rows come from all over HBM: start pulling this step's rows
       // into L2 now, a whole ring ahead of the gather (union pages of a query
       // block are shared by its queries and are L2-resident anyway)
-      if (more && row >= 0 && prm.mode != kModeQblock) {
+      if (more && row >= 0 && (prm.mode == kModeToken || prm.mode == kModePage)) {
         const char* rp = reinterpret_cast<const char*>(prm.kv + (size_t)row * prm.row_stride);
 #pragma unroll
         for (int l = 0; l < kDk * 2 / 128; ++l) prefetch_l2_line(rp + l * 128);
@@ -634,11 +655,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       // scaled, masked logits in place (log2 units); independent partial
       // maxima keep the dependency chains short
+      float sc = sl2;
+      if (kSoftCap) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          sa[j] = __float_as_uint(prm.cap_log2 * tanh_approx(__uint_as_float(sa[j]) * prm.inv_cap_scale));
+          sb[j] = __float_as_uint(prm.cap_log2 * tanh_approx(__uint_as_float(sb[j]) * prm.inv_cap_scale));
+        }
+        sc = 1.f;
+      }
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if ((mlo & mhi) == 0xffffffffu) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float a = __uint_as_float(sa[j]) * sl2, b = __uint_as_float(sb[j]) * sl2;
+          const float a = __uint_as_float(sa[j]) * sc, b = __uint_as_float(sb[j]) * sc;
           sa[j] = __float_as_uint(a);
           sb[j] = __float_as_uint(b);
           mx4[j & 1] = fmaxf(mx4[j & 1], a);
@@ -647,8 +677,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float a = ((mlo >> j) & 1u) ? __uint_as_float(sa[j]) * sl2 : -INFINITY;
-          const float b = ((mhi >> j) & 1u) ? __uint_as_float(sb[j]) * sl2 : -INFINITY;
+          const float a = ((mlo >> j) & 1u) ? __uint_as_float(sa[j]) * sc : -INFINITY;
+          const float b = ((mhi >> j) & 1u) ? __uint_as_float(sb[j]) * sc : -INFINITY;
           sa[j] = __float_as_uint(a);
           sb[j] = __float_as_uint(b);
           mx4[j & 1] = fmaxf(mx4[j & 1], a);
@@ -860,7 +890,7 @@ int attend_num_splits(int T, int H, int K, int mode) {
   if (mode == kModeQblock) return 1;
   const int ctas = T * 2 * ((H + 127) / 128);
   int z = max(1, sm_count() / max(1, ctas));
-  const int max_by_k = mode == kModeToken ? max(1, (K + 31) / 32) : max(1, K);
+  const int max_by_k = mode == kModeToken ? max(1, (K + 31) / 32) : max(1, K);  // dense: K = pages
   z = min(z, min(kMaxSplits, max_by_k));
   return max(1, z);
 }
@@ -895,9 +925,14 @@ int run_attend(cudaStream_t stream, AttendParams prm, void* ws, size_t ws_bytes)
   if (!encode_bf16_2d(&kvmap, prm.kv, (uint64_t)prm.P * prm.ps, (uint64_t)prm.row_stride, 32, kDk))
     return DSA_ERR_CUDA;
   if (!encode_bf16_2d(&qmap, prm.q, (uint64_t)prm.T * prm.H, kDk, 128, kDk)) return DSA_ERR_CUDA;
-  set_smem_attr_once(reinterpret_cast<const void*>(sparse_mla_kernel), kSmem);
   dim3 grid(cols, prm.T, prm.nsplit);
-  sparse_mla_kernel<<<grid, kThreads, kSmem, stream>>>(prm, kvmap, qmap);
+  if (prm.soft_cap_on) {
+    set_smem_attr_once(reinterpret_cast<const void*>(sparse_mla_kernel<true>), kSmem);
+    sparse_mla_kernel<true><<<grid, kThreads, kSmem, stream>>>(prm, kvmap, qmap);
+  } else {
+    set_smem_attr_once(reinterpret_cast<const void*>(sparse_mla_kernel<false>), kSmem);
+    sparse_mla_kernel<false><<<grid, kThreads, kSmem, stream>>>(prm, kvmap, qmap);
+  }
   DSA_CHECK_LAUNCH();
   return DSA_OK;
 }

@@ -6,7 +6,7 @@
 
 namespace dsa {
 
-enum : int { kModeToken = 0, kModePage = 1, kModeQblock = 2 };
+enum : int { kModeToken = 0, kModePage = 1, kModeQblock = 2, kModeDense = 3 };
 
 struct AttendParams {
   const uint16_t* q;   // bf16 [T, H, 576]
@@ -25,6 +25,10 @@ struct AttendParams {
   const uint32_t* member;
   const int32_t* counts;
   int QB, u_max;
+  int window;           // dense mode: keep the `window` most recent positions (0 = all)
+  int soft_cap_on;      // logits l -> cap * tanh(l / cap) before the softmax
+  float inv_cap_scale;  // sm_scale / cap
+  float cap_log2;       // cap * log2(e)
   int nsplit;
   uint16_t* o;      // bf16 [T, H, 512]
   float* lse;       // [T, H] or null

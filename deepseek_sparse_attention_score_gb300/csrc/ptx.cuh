@@ -301,6 +301,14 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// tanh with the hardware approximation (PTX tanh.approx, relative error
+// about 2^-11).
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ int warp_id() { return threadIdx.x >> 5; }
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 __device__ __forceinline__ bool elect_one() {

@@ -229,6 +229,25 @@ DSA_API int dsa_sparse_mla_prefill_qblock(dsa_stream_t stream, const uint16_t* q
                                   int32_t* dev_status);
 
 /* ------------------------------------------------------------------------
+ * Dense causal absorbed-MLA attention: the route the backend takes for
+ * layers without an indexer (dsa_sparse_backend.py, _run_dense, which calls
+ * the dense ragged paged MLA kernel with the layer's sliding window and
+ * logit soft cap; that kernel's module is not shown on the pages). For query
+ * t every position j with j < seq_len, j <= pos(t) and, when
+ * sliding_window > 0, j > pos(t) - sliding_window; with soft_cap > 0 each
+ * logit l = sm_scale * q.k becomes soft_cap * tanh(l / soft_cap) before the
+ * softmax. Output and lse as dsa_sparse_mla_decode.
+ *   max_kv  an upper bound on seq_lens (host-known), sizes the key splits
+ *   ws      workspace of dsa_sparse_mla_decode_workspace_size(T, H, Dv) bytes
+ * Supported: as dsa_sparse_mla_decode; sliding_window >= 0, soft_cap >= 0.
+ * ------------------------------------------------------------------------ */
+DSA_API int dsa_dense_mla(dsa_stream_t stream, const uint16_t* q, const uint16_t* kv, int row_stride,
+                          const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
+                          const int32_t* page_indices, int max_kv, int T, int S, int P, int PTW, int ps, int H,
+                          int Dk, int Dv, float sm_scale, int sliding_window, float soft_cap, uint16_t* o,
+                          float* lse, void* ws, size_t ws_bytes, int32_t* dev_status);
+
+/* ------------------------------------------------------------------------
  * Paged write-back of the new tokens' rows into a paged cache: the step
  * directly before the indexer and the attention, which read these rows.
  * dsa_sparse_backend.py, _scatter_paged (and the Pallas paged_write_back of

@@ -355,11 +355,18 @@ def qblock_attend(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, units, m
     return np.stack(os_), np.stack(ls)
 
 
-def dense_mla(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, sm_scale, Dv, tokens=None):
+def dense_mla(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, sm_scale, Dv, tokens=None,
+              sliding_window=None, soft_cap=None):
     """Dense causal absorbed-MLA (the route the backend falls back to): every
     visible position ``j < min(kv_len, pos+1)``, one position at a time, with
     a two-pass max/sum softmax. Written independently of ``sparse_mla`` so the
-    property "top-k with k >= kv_len equals dense attention" pins both."""
+    property "top-k with k >= kv_len equals dense attention" pins both.
+
+    The backend's dense route (dsa_sparse_backend.py, ``_run_dense``) also
+    passes the layer's ``sliding_window`` and ``logit_cap`` to the dense
+    kernel, whose module the pages do not show; the plain readings taken:
+    a window W keeps the W most recent positions ``pos - W < j <= pos``, and a
+    cap c maps each scaled logit l to ``c * tanh(l / c)`` before the softmax."""
     kvc = np.asarray(kv)
     P, ps, Dk_row = kvc.shape
     seq = token_seq(cu_q_lens)
@@ -374,16 +381,21 @@ def dense_mla(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, sm_scale, Dv
         H = qt.shape[0]
         Dk = qt.shape[-1]
         n = int(nvis[t])
-        if n == 0:
+        lo = 0
+        if sliding_window:
+            pos = n - 1  # the last visible position is the query's own
+            lo = max(0, pos - int(sliding_window) + 1)
+        if n - lo <= 0:
             out.append(np.zeros((H, Dv)))
             continue
         base = int(cu_kv_lens[s]) // ps
-        logit = np.empty((n, H))
-        vals = np.empty((n, Dv))
-        for j in range(n):
+        logit = np.empty((n - lo, H))
+        vals = np.empty((n - lo, Dv))
+        for j in range(lo, n):
             row = widen(kvc[pi[base + j // ps], j % ps])
-            logit[j] = sm_scale * (qt @ row[:Dk])
-            vals[j] = row[:Dv]
+            l = sm_scale * (qt @ row[:Dk])
+            logit[j - lo] = soft_cap * np.tanh(l / soft_cap) if soft_cap else l
+            vals[j - lo] = row[:Dv]
         mx = logit.max(axis=0)
         wgt = np.exp(logit - mx)
         out.append((wgt.T @ vals) / wgt.sum(axis=0)[:, None])

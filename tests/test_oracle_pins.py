@@ -440,3 +440,34 @@ def test_topk_pages_cover_exactly_the_selected_tokens():
     got = set(pages[pages >= 0].tolist())
     assert got == {int(j) // 64 for j in row} and n == len(got)
     assert all(a < b for a, b in zip(pages[:n], pages[1:n]))
+
+
+# ------------------------------------- dense MLA fallback: window and cap (NEXT-4)
+def test_dense_window_and_soft_cap_limits():
+    rng = np.random.default_rng(77)
+    q_lens, kv_lens = [1, 4, 2], [6, 11, 3]
+    q, kv, meta, Dv, ps = _mla_setup(rng, q_lens, kv_lens)
+    base = O.dense_mla(q, kv, **meta, sm_scale=0.3, Dv=Dv)
+    # a window at least as long as every context changes nothing
+    np.testing.assert_allclose(O.dense_mla(q, kv, **meta, sm_scale=0.3, Dv=Dv, sliding_window=64), base,
+                               rtol=1e-12, atol=1e-13)
+    # a huge cap is the identity on the logits
+    np.testing.assert_allclose(O.dense_mla(q, kv, **meta, sm_scale=0.3, Dv=Dv, soft_cap=1e9), base,
+                               rtol=1e-9, atol=1e-9)
+    seq = O.token_seq(meta["cu_q_lens"])
+    pos = O.token_pos(meta["seq_lens"], meta["cu_q_lens"])
+    kvf = O.widen(kv)
+    w1 = O.dense_mla(q, kv, **meta, sm_scale=0.3, Dv=Dv, sliding_window=1)
+    tiny = O.dense_mla(q, kv, **meta, sm_scale=0.3, Dv=Dv, soft_cap=1e-12)
+    w3 = O.dense_mla(q, kv, **meta, sm_scale=0.3, Dv=Dv, sliding_window=3, soft_cap=1e-12)
+    for t in range(sum(q_lens)):
+        s, p = int(seq[t]), int(pos[t])
+        rows = O.physical_rows(meta["cu_kv_lens"], meta["page_indices"], ps, s, np.arange(p + 1))
+        vals = kvf.reshape(-1, kvf.shape[-1])[rows, :Dv]
+        # window 1: only the query's own position -> its value, for every head
+        np.testing.assert_allclose(w1[t], np.tile(vals[-1], (w1.shape[1], 1)), rtol=1e-12, atol=1e-13)
+        # a vanishing cap flattens every logit -> the plain mean of the visible values
+        np.testing.assert_allclose(tiny[t], np.tile(vals.mean(axis=0), (tiny.shape[1], 1)), rtol=1e-9, atol=1e-9)
+        # both: the mean of the last three positions
+        np.testing.assert_allclose(w3[t], np.tile(vals[-3:].mean(axis=0), (w3.shape[1], 1)), rtol=1e-9,
+                                   atol=1e-9)
