@@ -248,6 +248,25 @@ def stage_roofline(wl, rn, timed):
         else:
             out["dense_mla"] = entry(timed(dense), 1152 * pairs, "hbm")
         out["dense_mla"]["in_step"] = False
+    # the approximate top-k (the pages' fast-path trade) on the decode rows,
+    # with its recall against the exact selection of the step
+    if not rn.prefill and rn.page_budget is None:
+        over = 4
+        ws_ap = torch.empty(max(1, dsa.lib().dsa_indexer_topk_approx_workspace_size(
+            rg.T, rg.S, int(rg.seq_lens.max()), ps, wl.k, over)), dtype=torch.uint8, device=rn.kv[0].device)
+        sel_ap = torch.empty((rg.T, wl.k), dtype=torch.int32, device=rn.kv[0].device)
+
+        def approx():
+            dsa.dsa_indexer_topk_approx(rn.q_idx, rn.w, rn.kcache[0], *rn.meta, k=wl.k, max_kv=int(rg.seq_lens.max()),
+                                        over=over, topk=sel_ap, ws=ws_ap, dev_status=rn.status)
+
+        e = entry(timed(approx), 256 * nvis.sum(), "hbm")
+        a, x = sel_ap.cpu().numpy(), rn.topk[0].cpu().numpy()
+        hit = sum(len(np.intersect1d(a[t][a[t] >= 0], x[t][x[t] >= 0])) for t in range(rg.T))
+        e["recall_vs_exact"] = hit / max(1, int((x >= 0).sum()))
+        e["over"] = over
+        e["in_step"] = False
+        out["indexer_topk_approx"] = e
     return out
 
 

@@ -43,6 +43,8 @@ EXPORTS = (
     "dsa_sparse_mla_prefill_qblock",
     "dsa_paged_write_back",
     "dsa_dense_mla",
+    "dsa_indexer_topk_approx_workspace_size",
+    "dsa_indexer_topk_approx",
     "dsa_topk_pages_from_tokens",
     "dsa_device_sm_count",
     "dsa_launch_count",
@@ -93,12 +95,16 @@ def lib() -> ctypes.CDLL:
     L.dsa_topk_pages_from_tokens.argtypes = [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P]
     L.dsa_dense_mla.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _F,
                                 _P, _P, _P, _Z, _P]
+    L.dsa_indexer_topk_approx_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I]
+    L.dsa_indexer_topk_approx_workspace_size.restype = _Z
+    L.dsa_indexer_topk_approx.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                                          _P, _P, _Z, _P]
     L.dsa_device_sm_count.argtypes = []
     L.dsa_launch_count.argtypes = []
     L.dsa_launch_count.restype = ctypes.c_longlong
     for name in EXPORTS:
         if name not in ("dsa_indexer_workspace_size", "dsa_sparse_mla_decode_workspace_size",
-                        "dsa_launch_count"):
+                        "dsa_launch_count", "dsa_indexer_topk_approx_workspace_size"):
             getattr(L, name).restype = _I
     _lib = L
     return L
@@ -397,3 +403,27 @@ def dsa_dense_mla(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, *, max_k
                              ws.numel(), _ptr(dev_status))
     _check("dsa_dense_mla", rc)
     return (o, lse) if lse is not None else o
+
+
+def dsa_indexer_topk_approx(q, w, kcache, seq_lens, cu_q_lens, cu_kv_lens, page_indices, *, k, max_kv, over=4,
+                            topk=None, ws=None, dev_status=None):
+    """Approximate token top-k: exact top-k of per-bin maxima over
+    ``min(n, over * k)`` strided bins of each score row (ascending
+    positions, -1 padded)."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev, 3)
+    _need(w, "w", torch.float32, dev, 2)
+    _need(kcache, "kcache", torch.bfloat16, dev, 3)
+    S, PTW = _meta(dev, seq_lens, cu_q_lens, cu_kv_lens, page_indices)
+    T, Hi, Di = q.shape
+    P, ps, _ = kcache.shape
+    if topk is None:
+        topk = torch.empty((T, k), dtype=torch.int32, device=dev)
+    if ws is None:
+        nb = lib().dsa_indexer_topk_approx_workspace_size(T, S, max_kv, ps, k, over)
+        ws = torch.empty(max(1, nb), dtype=torch.uint8, device=dev)
+    rc = lib().dsa_indexer_topk_approx(_stream(dev), _ptr(q), _ptr(w), _ptr(kcache), _ptr(seq_lens), _ptr(cu_q_lens),
+                                       _ptr(cu_kv_lens), _ptr(page_indices), T, S, P, PTW, ps, Hi, Di, int(max_kv),
+                                       int(k), int(over), _ptr(topk), _ptr(ws), ws.numel(), _ptr(dev_status))
+    _check("dsa_indexer_topk_approx", rc)
+    return topk

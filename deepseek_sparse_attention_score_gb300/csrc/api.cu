@@ -189,6 +189,56 @@ size_t dsa_indexer_workspace_size(int T, int S, int max_kv, int ps) {
   return indexer_layout(T, S, max_kv, ps).total;
 }
 
+// workspace of the approximate top-k: the indexer's, then bin maxima and
+// their positions [T, B], bin counts [T] and the selected bins [T, k]
+static size_t approx_bins(int k, int over, int max_kv) {
+  const long long kb = (long long)k * over;
+  return (size_t)(kb < max_kv ? kb : max_kv);
+}
+static size_t approx_extra(int T, int k, int over, int max_kv) {
+  const size_t B = approx_bins(k, over, max_kv);
+  return 2 * align_up((size_t)T * B * 4, 256) + align_up((size_t)T * 4, 256) + align_up((size_t)T * k * 4, 256);
+}
+
+size_t dsa_indexer_topk_approx_workspace_size(int T, int S, int max_kv, int ps, int k, int over) {
+  if (T < 0 || S < 0 || max_kv < 1 || !ps_supported(ps) || k < 1 || over < 1) return 0;
+  return indexer_layout(T, S, max_kv, ps).total + approx_extra(T, k, over, max_kv);
+}
+
+int dsa_indexer_topk_approx(dsa_stream_t stream, const uint16_t* q, const float* w, const uint16_t* kcache,
+                            const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
+                            const int32_t* page_indices, int T, int S, int P, int PTW, int ps, int Hi, int Di,
+                            int max_kv, int k, int over, int32_t* topk, void* ws, size_t ws_bytes,
+                            int32_t* dev_status) {
+  int rc = check_meta(seq_lens, cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps);
+  if (rc) return rc;
+  if (Hi != 32 || Di != 128) return DSA_ERR_UNSUPPORTED;
+  if (!topk || k < 1 || over < 1 || max_kv < 1) return DSA_ERR_INVALID_ARGUMENT;
+  if (k > approx_max_k()) return DSA_ERR_UNSUPPORTED;
+  if (T == 0) return DSA_OK;
+  if (!q || !w || !kcache) return DSA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(w) || !aligned16(kcache)) return DSA_ERR_ALIGNMENT;
+  if (T >= (1 << 24) || S >= (1 << 24)) return DSA_ERR_UNSUPPORTED;
+  const IndexerLayout L = indexer_layout(T, S, max_kv, ps);
+  if (!ws || ws_bytes < L.total + approx_extra(T, k, over, max_kv) || !aligned16(ws)) return DSA_ERR_WORKSPACE;
+  IndexerMeta m{w, seq_lens, cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps, max_kv, dev_status};
+  IndexerPlan pl;
+  IndexerOut out;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  rc = run_indexer(st, m, q, kcache, ws, L, true, false, &pl, &out);
+  if (rc) return rc;
+  const size_t B = approx_bins(k, over, max_kv);
+  uint8_t* x = static_cast<uint8_t*>(ws) + L.total;
+  float* vals = reinterpret_cast<float*>(x);
+  x += align_up((size_t)T * B * 4, 256);
+  int* pos = reinterpret_cast<int*>(x);
+  x += align_up((size_t)T * B * 4, 256);
+  int* nb = reinterpret_cast<int*>(x);
+  x += align_up((size_t)T * 4, 256);
+  int32_t* cand = reinterpret_cast<int32_t*>(x);
+  return run_topk_approx(st, out.tok_scores, out.ld_tok, pl.nvis, T, k, over, max_kv, vals, pos, nb, cand, topk);
+}
+
 int dsa_indexer_topk(dsa_stream_t stream, const uint16_t* q, const float* w, const uint16_t* kcache,
                      const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
                      const int32_t* page_indices, int T, int S, int P, int PTW, int ps, int Hi, int Di, int max_kv,

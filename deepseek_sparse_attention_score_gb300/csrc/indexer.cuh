@@ -44,6 +44,10 @@ IndexerLayout indexer_layout(int T, int S, int max_kv, int ps);
 int run_indexer(cudaStream_t stream, const IndexerMeta& m, const uint16_t* q, const uint16_t* kcache, void* ws,
                 const IndexerLayout& L, bool want_tok, bool want_page, IndexerPlan* plan_out, IndexerOut* out_out);
 
+// Approximate token top-k over the score rows (approx.cu).
+int approx_max_k();
+int run_topk_approx(cudaStream_t stream, const float* scores, long long ld, const int* nvis, int T, int k, int over,
+                    int max_kv, float* vals, int* pos, int* nb, int32_t* cand, int32_t* out);
 // Exact per-row top-k over a score buffer (token or page scores).
 int run_topk(cudaStream_t stream, const float* scores, long long ld, const int* nvis, int T, int div, int k,
              int32_t* out_idx, float* out_val, int max_len);

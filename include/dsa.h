@@ -229,6 +229,26 @@ DSA_API int dsa_sparse_mla_prefill_qblock(dsa_stream_t stream, const uint16_t* q
                                   int32_t* dev_status);
 
 /* ------------------------------------------------------------------------
+ * Approximate token top-k (the trade the pages make with approx_max_k on
+ * their fast path; ref.py, streamindex_topk_ref is the exact definition).
+ * Scores as dsa_indexer_topk. A row of n visible scores is folded into
+ * B = min(n, over*k) bins (bin b holds positions b, b+B, b+2B, ...); each
+ * bin keeps its largest score (lowest position on ties); the selection is
+ * the exact top-k of the B bin maxima (ties to the lower bin), written as
+ * ascending positions, -1 padded. count = min(k, n); over*k >= n makes it
+ * the exact top-k up to ties; a larger `over` raises the recall.
+ *   ws  workspace of dsa_indexer_topk_approx_workspace_size(T, S, max_kv,
+ *       ps, k, over) bytes
+ * Supported: as dsa_indexer_topk, k <= 16384, over >= 1.
+ * ------------------------------------------------------------------------ */
+DSA_API size_t dsa_indexer_topk_approx_workspace_size(int T, int S, int max_kv, int ps, int k, int over);
+DSA_API int dsa_indexer_topk_approx(dsa_stream_t stream, const uint16_t* q, const float* w, const uint16_t* kcache,
+                                    const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
+                                    const int32_t* page_indices, int T, int S, int P, int PTW, int ps, int Hi,
+                                    int Di, int max_kv, int k, int over, int32_t* topk, void* ws, size_t ws_bytes,
+                                    int32_t* dev_status);
+
+/* ------------------------------------------------------------------------
  * Dense causal absorbed-MLA attention: the route the backend takes for
  * layers without an indexer (dsa_sparse_backend.py, _run_dense, which calls
  * the dense ragged paged MLA kernel with the layer's sliding window and

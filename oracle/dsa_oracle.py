@@ -439,3 +439,29 @@ def topk_pages_of_tokens(topk_row, ps, cap):
     n = min(cap, len(uniq))
     out[:n] = uniq[:n]
     return out, len(uniq)
+
+
+def approx_topk_of_row(scores, k, over):
+    """Approximate top-k of one score row (the pages' fast path uses
+    ``approx_max_k`` with a recall target; this is the two-stage form the
+    build implements, written out): fold the n scores into
+    ``B = min(n, over*k)`` bins (bin b holds positions b, b+B, ...), keep each
+    bin's largest score (lowest position on ties), take the exact top-k of
+    the B bin maxima (ties to the lower bin) and return their positions in
+    ascending order, -1 padded."""
+    s = np.asarray(scores, dtype=np.float32)
+    n = len(s)
+    out = np.full(k, -1, dtype=np.int64)
+    if n == 0:
+        return out
+    B = min(n, over * k)
+    best_pos = np.empty(B, dtype=np.int64)
+    best_val = np.empty(B, dtype=np.float32)
+    for b in range(B):
+        idx = np.arange(b, n, B)
+        j = idx[int(np.argmax(s[idx]))]  # argmax returns the first (lowest) maximum
+        best_pos[b], best_val[b] = j, s[j]
+    bins = topk_of_row(best_val, k)
+    sel = np.sort(best_pos[bins[bins >= 0]])
+    out[: len(sel)] = sel
+    return out

@@ -471,3 +471,37 @@ def test_dense_window_and_soft_cap_limits():
         # both: the mean of the last three positions
         np.testing.assert_allclose(w3[t], np.tile(vals[-3:].mean(axis=0), (w3.shape[1], 1)), rtol=1e-9,
                                    atol=1e-9)
+
+
+# --------------------------------------------- approximate top-k (NEXT-3)
+def test_approx_topk_hand_example_and_exact_limit():
+    s = np.array([5, 1, 9, 3, 2, 8, 7, 0], np.float32)
+    # k=2, over=2 -> 4 bins {0,4} {1,5} {2,6} {3,7}: maxima 5@0, 8@5, 9@2, 3@3
+    # -> best two bins hold 9@2 and 8@5
+    assert O.approx_topk_of_row(s, 2, 2).tolist() == [2, 5]
+    # k=3, over=1 -> 3 bins {0,3,6} {1,4,7} {2,5}: maxima 7@6, 2@4, 9@2 -> all three bins
+    assert O.approx_topk_of_row(s, 3, 1).tolist() == [2, 4, 6]
+    rng = np.random.default_rng(9)
+    for n in (1, 17, 300):
+        x = rng.standard_normal(n).astype(np.float32)
+        for k in (1, 5, 64):
+            # enough bins for every position: the exact top-k
+            assert O.approx_topk_of_row(x, k, max(1, -(-n // k))).tolist() == O.topk_of_row(x, k).tolist()
+
+
+def test_approx_topk_selects_bin_maxima_and_count():
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal(5000).astype(np.float32)
+    k, over = 64, 4
+    sel = O.approx_topk_of_row(x, k, over)
+    assert (sel >= 0).sum() == k and np.all(np.diff(sel) > 0)
+    B = over * k
+    exact = set(O.topk_of_row(x, k).tolist())
+    for j in sel:
+        bin_idx = np.arange(j % B, 5000, B)
+        assert x[j] == x[bin_idx].max()
+    # every exact winner that is the maximum of its bin is found
+    for j in exact:
+        bin_idx = np.arange(j % B, 5000, B)
+        if x[j] == x[bin_idx].max():
+            assert j in set(sel.tolist())
