@@ -49,6 +49,8 @@ constexpr int kPlanStageS = 4096;  // requests whose query offsets the planner k
 __global__ void __launch_bounds__(1024) indexer_plan_kernel(IndexerMeta m, IndexerPlan pl, int ch1, int ch8) {
   __shared__ int s_warp[32];
   __shared__ int s_cuq[kPlanStageS + 1];
+  __shared__ int s_off[1024];
+  __shared__ int4 s_tile[1024];
   const int T = m.T, S = m.S, ps = m.ps;
   // token -> request searches run against a shared-memory copy of cu_q_lens
   // when it fits (a chain of dependent global loads otherwise)
@@ -133,10 +135,23 @@ __global__ void __launch_bounds__(1024) indexer_plan_kernel(IndexerMeta m, Index
       }
       int tot;
       const int e = block_excl_scan(n, s_warp, &tot);
-      for (int c = 0; c < n; ++c) {
-        const int kb = c * ch, ke = min(tl.w, kb + ch);
-        items[carry + e + c] = make_int4(tl.x, (tl.y << 24) | tl.z, kb, ke);
+      // every thread writes items (coalesced), finding its tile by a search
+      // over this batch's item offsets
+      s_off[threadIdx.x] = i < ntiles ? e : 0x7fffffff;
+      s_tile[threadIdx.x] = tl;
+      __syncthreads();
+      const int nb = min((int)blockDim.x, ntiles - i0);
+      for (int j = threadIdx.x; j < tot; j += blockDim.x) {
+        int lo = 0, hi = nb - 1;  // last tile whose offset is <= j
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (s_off[mid] <= j) lo = mid; else hi = mid - 1;
+        }
+        const int4 tj = s_tile[lo];
+        const int kb = (j - s_off[lo]) * ch, ke = min(tj.w, kb + ch);
+        items[carry + j] = make_int4(tj.x, (tj.y << 24) | tj.z, kb, ke);
       }
+      __syncthreads();
       carry += tot;
     }
     if (threadIdx.x == 0) pl.counts[list] = carry;
