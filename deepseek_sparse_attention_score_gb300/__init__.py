@@ -17,6 +17,7 @@ from .abi import (  # noqa: F401
     dsa_sparse_mla_decode_noalloc,
     dsa_paged_write_back,
     dsa_dense_mla,
+    dsa_selftest_wait_timeout,
     dsa_indexer_topk_approx,
     dsa_topk_pages_from_tokens,
     dsa_sparse_mla_decode_workspace_size,

@@ -43,6 +43,7 @@ EXPORTS = (
     "dsa_sparse_mla_prefill_qblock",
     "dsa_paged_write_back",
     "dsa_dense_mla",
+    "dsa_selftest_wait_timeout",
     "dsa_indexer_topk_approx_workspace_size",
     "dsa_indexer_topk_approx",
     "dsa_topk_pages_from_tokens",
@@ -99,6 +100,7 @@ def lib() -> ctypes.CDLL:
     L.dsa_indexer_topk_approx_workspace_size.restype = _Z
     L.dsa_indexer_topk_approx.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I,
                                           _P, _P, _Z, _P]
+    L.dsa_selftest_wait_timeout.argtypes = [_P, ctypes.c_longlong, _P]
     L.dsa_device_sm_count.argtypes = []
     L.dsa_launch_count.argtypes = []
     L.dsa_launch_count.restype = ctypes.c_longlong
@@ -427,3 +429,11 @@ def dsa_indexer_topk_approx(q, w, kcache, seq_lens, cu_q_lens, cu_kv_lens, page_
                                        int(k), int(over), _ptr(topk), _ptr(ws), ws.numel(), _ptr(dev_status))
     _check("dsa_indexer_topk_approx", rc)
     return topk
+
+
+def dsa_selftest_wait_timeout(dev_status, limit_clocks=2_000_000):
+    """Run one bounded wait that is bound to run out (a barrier nothing
+    arrives on); the device status word gets DSA_STATUS_TIMEOUT."""
+    _need(dev_status, "dev_status", torch.int32, dev_status.device, 1)
+    rc = lib().dsa_selftest_wait_timeout(_stream(dev_status.device), int(limit_clocks), _ptr(dev_status))
+    _check("dsa_selftest_wait_timeout", rc)

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB_NAME = "libdsa_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
-SOURCES = ["api.cu", "indexer.cu", "topk.cu", "union.cu", "attend.cu", "writeback.cu", "pages.cu", "approx.cu"]
+SOURCES = ["api.cu", "indexer.cu", "topk.cu", "union.cu", "attend.cu", "writeback.cu", "pages.cu", "approx.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-diag-suppress", "177"]

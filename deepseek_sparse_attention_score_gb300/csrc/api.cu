@@ -6,6 +6,8 @@
 #include <cmath>
 #include <cstdint>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "attend.cuh"
 #include "common.cuh"
 #include "indexer.cuh"
@@ -132,12 +134,27 @@ static int attend_check(const uint16_t* q, const uint16_t* kv, int row_stride, i
 
 using namespace dsa;
 
+namespace {
+// One NVTX range per device entry point, so a timeline tool shows the ABI
+// calls around their kernels (header-only NVTX: free unless a tool attaches).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+}  // namespace
+
 extern "C" {
 
 int dsa_device_sm_count(void) { return sm_count(); }
 
+int dsa_selftest_wait_timeout(dsa_stream_t stream, long long limit_clocks, int32_t* dev_status) {
+  if (!dev_status || limit_clocks < 1 || limit_clocks > 10000000000LL) return DSA_ERR_INVALID_ARGUMENT;
+  return run_wait_timeout_selftest(static_cast<cudaStream_t>(stream), limit_clocks, dev_status);
+}
+
 int dsa_topk_pages_from_tokens(dsa_stream_t stream, const int32_t* topk, int T, int K, int ps, int max_pages,
                                int cap, int32_t* pages, int32_t* counts, int32_t* dev_status) {
+  NvtxRange nvtx_range("dsa_topk_pages_from_tokens");
   if (T < 0 || K < 0 || ps < 1 || cap < 1) return DSA_ERR_INVALID_ARGUMENT;
   if (max_pages < 1 || max_pages > topk_pages_max_pages()) return DSA_ERR_UNSUPPORTED;
   if (T == 0) return DSA_OK;
@@ -150,6 +167,7 @@ int dsa_paged_write_back(dsa_stream_t stream, const uint16_t* rows, int src_stri
                          int cache_stride, const int32_t* seq_lens, const int32_t* cu_q_lens,
                          const int32_t* cu_kv_lens, const int32_t* page_indices, int T, int S, int P, int PTW,
                          int ps, int32_t* dev_status) {
+  NvtxRange nvtx_range("dsa_paged_write_back");
   if (T < 0 || S < 0 || P < 0 || PTW < 0 || D < 0) return DSA_ERR_INVALID_ARGUMENT;
   if (T == 0 || D == 0) return DSA_OK;
   if (S < 1 || P < 1 || PTW < 1 || ps < 1) return DSA_ERR_INVALID_ARGUMENT;
@@ -210,6 +228,7 @@ int dsa_indexer_topk_approx(dsa_stream_t stream, const uint16_t* q, const float*
                             const int32_t* page_indices, int T, int S, int P, int PTW, int ps, int Hi, int Di,
                             int max_kv, int k, int over, int32_t* topk, void* ws, size_t ws_bytes,
                             int32_t* dev_status) {
+  NvtxRange nvtx_range("dsa_indexer_topk_approx");
   int rc = check_meta(seq_lens, cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps);
   if (rc) return rc;
   if (Hi != 32 || Di != 128) return DSA_ERR_UNSUPPORTED;
@@ -243,6 +262,7 @@ int dsa_indexer_topk(dsa_stream_t stream, const uint16_t* q, const float* w, con
                      const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
                      const int32_t* page_indices, int T, int S, int P, int PTW, int ps, int Hi, int Di, int max_kv,
                      int k, int32_t* topk, float* topk_scores, void* ws, size_t ws_bytes, int32_t* dev_status) {
+  NvtxRange nvtx_range("dsa_indexer_topk");
   if (!topk) return DSA_ERR_INVALID_ARGUMENT;
   return indexer_common(static_cast<cudaStream_t>(stream), q, w, kcache, seq_lens, cu_q_lens, cu_kv_lens,
                         page_indices, T, S, P, PTW, ps, Hi, Di, max_kv, 0, nullptr, k, topk, topk_scores, ws,
@@ -254,6 +274,7 @@ int dsa_indexer_page_topk(dsa_stream_t stream, const uint16_t* q, const float* w
                           const int32_t* page_indices, int T, int S, int P, int PTW, int ps, int Hi, int Di,
                           int max_kv, int k_pages, int32_t* topk_pages, int k, int32_t* topk, float* topk_scores,
                           void* ws, size_t ws_bytes, int32_t* dev_status) {
+  NvtxRange nvtx_range("dsa_indexer_page_topk");
   if (!topk_pages) return DSA_ERR_INVALID_ARGUMENT;
   return indexer_common(static_cast<cudaStream_t>(stream), q, w, kcache, seq_lens, cu_q_lens, cu_kv_lens,
                         page_indices, T, S, P, PTW, ps, Hi, Di, max_kv, k_pages, topk_pages, k, topk, topk_scores,
@@ -263,6 +284,7 @@ int dsa_indexer_page_topk(dsa_stream_t stream, const uint16_t* q, const float* w
 int dsa_build_block_union(dsa_stream_t stream, const int32_t* topk_units, int T, int K, int QB, int u_max,
                           const int32_t* cu_q_lens, const int32_t* cu_kv_lens, int S, int ps, int PTW,
                           int32_t* units, uint32_t* member, int32_t* counts, int32_t* dev_status) {
+  NvtxRange nvtx_range("dsa_build_block_union");
   if (T < 0 || K < 1 || QB < 32 || QB % 32 != 0 || QB > 1024 || PTW < 1) return DSA_ERR_INVALID_ARGUMENT;
   if (cu_q_lens && (!cu_kv_lens || S < 1 || ps < 1)) return DSA_ERR_INVALID_ARGUMENT;
   if (u_max <= 0) u_max = (int)std::min<long long>((long long)QB * K, PTW);
@@ -283,6 +305,7 @@ int dsa_sparse_mla_decode(dsa_stream_t stream, const uint16_t* q, const uint16_t
                           const int32_t* page_indices, const int32_t* sel, int K, int unit, int T, int S, int P,
                           int PTW, int ps, int H, int Dk, int Dv, float sm_scale, uint16_t* o, float* lse,
                           void* ws, size_t ws_bytes, int32_t* dev_status) {
+  NvtxRange nvtx_range("dsa_sparse_mla_decode");
   int rc = check_meta(seq_lens, cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps);
   if (rc) return rc;
   rc = attend_check(q, kv, row_stride, T, H, Dk, Dv, o);
@@ -325,6 +348,7 @@ int dsa_dense_mla(dsa_stream_t stream, const uint16_t* q, const uint16_t* kv, in
                   const int32_t* cu_q_lens, const int32_t* cu_kv_lens, const int32_t* page_indices, int max_kv,
                   int T, int S, int P, int PTW, int ps, int H, int Dk, int Dv, float sm_scale, int sliding_window,
                   float soft_cap, uint16_t* o, float* lse, void* ws, size_t ws_bytes, int32_t* dev_status) {
+  NvtxRange nvtx_range("dsa_dense_mla");
   int rc = check_meta(seq_lens, cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps);
   if (rc) return rc;
   rc = attend_check(q, kv, row_stride, T, H, Dk, Dv, o);
@@ -369,6 +393,7 @@ int dsa_sparse_mla_decode_noalloc(dsa_stream_t stream, const uint16_t* q, const 
                                   const int32_t* page_indices, const int32_t* sel, int K, int unit, int T, int S,
                                   int P, int PTW, int ps, int H, int Dk, int Dv, float sm_scale, uint16_t* o,
                                   float* lse, int32_t* dev_status) {
+  NvtxRange nvtx_range("dsa_sparse_mla_decode_noalloc");
   int rc = check_meta(seq_lens, cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps);
   if (rc) return rc;
   rc = attend_check(q, kv, row_stride, T, H, Dk, Dv, o);
@@ -408,6 +433,7 @@ int dsa_sparse_mla_prefill_qblock(dsa_stream_t stream, const uint16_t* q, const 
                                   const int32_t* counts, int QB, int u_max, int T, int S, int P, int PTW, int ps,
                                   int H, int Dk, int Dv, float sm_scale, uint16_t* o, float* lse,
                                   int32_t* dev_status) {
+  NvtxRange nvtx_range("dsa_sparse_mla_prefill_qblock");
   int rc = check_meta(seq_lens, cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps);
   if (rc) return rc;
   rc = attend_check(q, kv, row_stride, T, H, Dk, Dv, o);

@@ -59,4 +59,7 @@ int topk_pages_max_pages();
 int run_topk_pages(cudaStream_t stream, const int32_t* topk, int T, int K, int ps, int max_pages, int cap,
                    int32_t* pages, int32_t* counts, int32_t* dev_status);
 
+// Bounded-wait self-test (selftest.cu).
+int run_wait_timeout_selftest(cudaStream_t stream, long long limit_clocks, int32_t* dev_status);
+
 }  // namespace dsa

@@ -61,17 +61,21 @@ constexpr uint32_t kWaitSleepNs = 20000;
 // Bounded wait on the phase with the given parity. Returns false when the CTA
 // is aborting (``abort_flag`` set by another thread) or when this wait timed
 // out, in which case it sets the flag itself.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                long long limit_clocks) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitTimeoutClocks) {
+    if (clock64() - t0 > limit_clocks) {
       *abort_flag = 1;
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  return mbar_wait_limit(bar, parity, abort_flag, kWaitTimeoutClocks);
 }
 
 // Bounded wait that ignores the abort flag: used while unwinding, to let

@@ -310,6 +310,15 @@ DSA_API int dsa_topk_pages_from_tokens(dsa_stream_t stream, const int32_t* topk,
                                        int max_pages, int cap, int32_t* pages, int32_t* counts,
                                        int32_t* dev_status);
 
+/* Self-test of failure detection; the source pages have no counterpart.
+ * Every pipeline wait in these kernels is bounded: when it runs out, the CTA
+ * sets DSA_STATUS_TIMEOUT in the status word, unwinds and returns instead of
+ * hanging or trapping. This entry runs one such wait on a barrier that
+ * nothing arrives on, bounded by limit_clocks SM clocks (1 .. 1e10), so a
+ * test can check that the status is set and the context stays usable.
+ *   dev_status  device int32, required */
+DSA_API int dsa_selftest_wait_timeout(dsa_stream_t stream, long long limit_clocks, int32_t* dev_status);
+
 /* Number of streaming multiprocessors the kernels size their grids for
  * (device of the current context); a query helper, no device work. */
 DSA_API int dsa_device_sm_count(void);

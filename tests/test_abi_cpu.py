@@ -67,3 +67,13 @@ def test_workspace_sizes_are_host_computable(dsa):
     b = dsa.dsa_indexer_workspace_size(64, 32, 8192, 64)
     assert 0 < a < b
     assert dsa.dsa_indexer_workspace_size(32, 32, 8192, 48) == 0  # unsupported page size
+
+
+def test_selftest_wait_timeout_validates_on_host(dsa):
+    import ctypes
+
+    L = dsa.lib()
+    fake = ctypes.c_void_p(16)  # never dereferenced: the arguments are rejected first
+    assert L.dsa_selftest_wait_timeout(None, 0, fake) == -1
+    assert L.dsa_selftest_wait_timeout(None, 10**11, fake) == -1
+    assert L.dsa_selftest_wait_timeout(None, 1000, None) == -1
