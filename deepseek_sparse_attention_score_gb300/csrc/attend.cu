@@ -69,6 +69,12 @@ constexpr uint32_t kColS = 128;  // two S buffers of 64 fp32 columns; P (bf16 pa
 constexpr uint32_t kColO = 256;  // 256 fp32 columns
 constexpr float kRescaleThreshold = 8.f;  // log2 units: p stays <= 256
 constexpr int kMaxSplits = 8;
+// epilogue stage: 128 rows of 256 fp32 values, rows padded to 1040 bytes so
+// that eight lanes writing eight rows hit eight different bank groups
+constexpr int kStageLd = kDvHalf + 4;
+constexpr int OFF_STAGE = 0;
+constexpr int OFF_WTS = OFF_STAGE + 128 * kStageLd * 4;  // fp32 merge weights [kMaxSplits][128]
+static_assert(OFF_WTS + kMaxSplits * 128 * 4 <= OFF_VST, "the stage must stay clear of the value stages");
 // every full barrier completes after two generator steps' worth of arrivals:
 // each gather thread once per step, plus one more by the leader per step
 constexpr uint32_t kFullArrivals = 2 * (kCopyThreads + 1);
@@ -96,11 +102,13 @@ struct TileGen {
   int w_phys;         // this lane's unit: physical page, -1 if none
   int cur_key0, cur_phys, sub, cur_valid;
   int b, qq, cnt;     // qblock
+  int ps_log2;        // the page size is a power of two
   int key_lo;         // dense: first key position inside the window
 
   __device__ void init(const AttendParams& prm, int tok, int split) {
     p = &prm;
     mode = prm.mode;
+    ps_log2 = 31 - __clz(prm.ps);
     t = tok;
     const int sq = seq_of_token_warp(prm.cu_q_lens, prm.S, tok);
     TokenGeom g = token_geom(prm.seq_lens, prm.cu_q_lens, prm.cu_kv_lens, prm.S, prm.ps, 0x3fffffff, tok,
@@ -168,14 +176,14 @@ struct TileGen {
         }
         int pg[GB];
 #pragma unroll
-        for (int g = 0; g < GB; ++g) pg[g] = (j[g] >= 0 && j[g] < n_vis) ? page_of(page_base + j[g] / ps) : -1;
+        for (int g = 0; g < GB; ++g) pg[g] = (j[g] >= 0 && j[g] < n_vis) ? page_of(page_base + (j[g] >> ps_log2)) : -1;
         // every array index below is a compile-time constant, so the buffer
         // stays in registers
 #pragma unroll
         for (int g = 0; g < GB; ++g) {
           const bool v = pg[g] >= 0;
           const uint32_t m = __ballot_sync(0xffffffffu, v);
-          buf_row[g] = v ? pg[g] * ps + j[g] % ps : -1;
+          buf_row[g] = v ? pg[g] * ps + (j[g] & (ps - 1)) : -1;
           buf_mask[g] = m;
           buf_pend |= (m ? 1u : 0u) << g;
         }
@@ -427,7 +435,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                   t * prm.H + h0);
   }
   // The key generator (warp 1) resolves its first window of selections while
-  // Q arrives; it publishes steps only after the barrier below.
+  // Q arrives; it publishes steps only after the barrier below. (Measured:
+  // calling TileGen::next from the generator loop alone, which halves its
+  // inlined code, made the query-block prefill 60% slower; the time of this
+  // kernel follows its code layout as much as its instruction count.)
   TileGen gen;
   bool gen_more = false;
   long long gen_row = -1, gen_base = -1;
@@ -734,7 +745,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = h0 + r;
     const bool hv = h < prm.H;
     const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-    const size_t orow = ((size_t)t * prm.H + h) * kDv + half * kDvHalf;
     const float lse_v = l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
     const bool have_o = n > 0 && ok;
     // O is read back from TMEM 64 columns at a time (one wait per two loads)
@@ -759,7 +769,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
     };
+    auto store_bf16_4 = [&](uint16_t* dst, float4 a) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
+      *reinterpret_cast<uint2*>(dst) = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+    };
     if (prm.nsplit == 1) {
+      // one split: each thread stores its own head row (measured faster here
+      // than the staged, line-wide stores of the split path below)
+      const size_t orow = ((size_t)t * prm.H + h) * kDv + half * kDvHalf;
 #pragma unroll 1
       for (int c0 = 0; c0 < kDvHalf; c0 += 64) {
         uint32_t oa[32], ob[32];
@@ -773,22 +790,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       // split keys: write this split's normalised partial; the last CTA of the
       // (token, value half) group merges all splits and writes the output.
-      float* op = prm.o_part + ((size_t)split * prm.T * prm.H) * kDv;
+      // O leaves TMEM through shared memory: each thread puts its head row
+      // (scaled by 1/l) into its warp's slice of the stage, then the warp
+      // writes one row at a time, 32 lanes over consecutive 16-byte pieces,
+      // so that every store and every load of the merge covers whole cache
+      // lines. The stage reuses the Q and key buffers, idle once the last PV
+      // has completed.
+      float* stg = reinterpret_cast<float*>(smem + OFF_STAGE) + (warp & 3) * 32 * kStageLd;
 #pragma unroll 1
       for (int c0 = 0; c0 < kDvHalf; c0 += 64) {
         uint32_t oa[32], ob[32];
         load_o64(c0, oa, ob);
-        if (hv) {
-          float4* dst = reinterpret_cast<float4*>(op + orow + c0);
+        float4* srow = reinterpret_cast<float4*>(stg + lane * kStageLd + c0);
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[v] = make_float4(__uint_as_float(oa[4 * v]) * inv_l, __uint_as_float(oa[4 * v + 1]) * inv_l,
-                                 __uint_as_float(oa[4 * v + 2]) * inv_l, __uint_as_float(oa[4 * v + 3]) * inv_l);
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[8 + v] = make_float4(__uint_as_float(ob[4 * v]) * inv_l, __uint_as_float(ob[4 * v + 1]) * inv_l,
-                                     __uint_as_float(ob[4 * v + 2]) * inv_l, __uint_as_float(ob[4 * v + 3]) * inv_l);
+        for (int v = 0; v < 8; ++v) {
+          srow[v] = make_float4(__uint_as_float(oa[4 * v]) * inv_l, __uint_as_float(oa[4 * v + 1]) * inv_l,
+                                __uint_as_float(oa[4 * v + 2]) * inv_l, __uint_as_float(oa[4 * v + 3]) * inv_l);
+          srow[8 + v] = make_float4(__uint_as_float(ob[4 * v]) * inv_l, __uint_as_float(ob[4 * v + 1]) * inv_l,
+                                    __uint_as_float(ob[4 * v + 2]) * inv_l, __uint_as_float(ob[4 * v + 3]) * inv_l);
         }
+      }
+      __syncwarp();
+      // rows of this warp that exist (h < H); uniform over the warp
+      const int hw = h0 + (warp & 3) * 32;
+      const int nrows = max(0, min(32, prm.H - hw));
+      const size_t orow0 = ((size_t)t * prm.H + hw) * kDv + half * kDvHalf;  // element offset of row hw
+      float* op = prm.o_part + ((size_t)split * prm.T * prm.H) * kDv + orow0;
+#pragma unroll 2
+      for (int i = 0; i < nrows; ++i) {
+        const float* sr = stg + i * kStageLd;
+        float4* dst = reinterpret_cast<float4*>(op + (size_t)i * kDv);
+        dst[lane] = *reinterpret_cast<const float4*>(sr + 4 * lane);
+        dst[32 + lane] = *reinterpret_cast<const float4*>(sr + 128 + 4 * lane);
       }
       // lse of this split as seen by this CTA (both value halves compute the
       // same logits, so each group merges with its own copies)
@@ -805,70 +838,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         *s_last = last;
       }
       named_bar_sync(2, 128);
-      if (*s_last) {  // uniform over the CTA: the TMEM reads below are warp-wide
+      if (*s_last) {  // uniform over the CTA
         __threadfence();
-        float wz[kMaxSplits];
+        // per head row (this thread's): the weight of each split's partial,
+        // kept in shared memory for the warp-wide merge below
+        float* wts = reinterpret_cast<float*>(smem + OFF_WTS);
+        auto lse_of = [&](int z) {
+          return __ldcg(lsep + (((size_t)z * prm.T + t) * gridDim.x + blockIdx.x) * 128 + r);
+        };
         float mx = -INFINITY;
-#pragma unroll
-        for (int z = 0; z < kMaxSplits; ++z) {
-          if (z >= prm.nsplit) break;
-          wz[z] = __ldcg(lsep + (((size_t)z * prm.T + t) * gridDim.x + blockIdx.x) * 128 + r);
-          mx = fmaxf(mx, wz[z]);
-        }
+#pragma unroll 1
+        for (int z = 0; z < prm.nsplit; ++z) mx = fmaxf(mx, lse_of(z));
         float tot = 0.f;
-#pragma unroll
-        for (int z = 0; z < kMaxSplits; ++z) {
-          if (z < prm.nsplit) {
-            wz[z] = (mx == -INFINITY || wz[z] == -INFINITY) ? 0.f : exp2f((wz[z] - mx) * 1.4426950408889634f);
-            tot += wz[z];
-          }
+#pragma unroll 1
+        for (int z = 0; z < prm.nsplit; ++z) {
+          const float lz = lse_of(z);
+          const float w = (mx == -INFINITY || lz == -INFINITY) ? 0.f : exp2f((lz - mx) * 1.4426950408889634f);
+          wts[z * 128 + r] = w;
+          tot += w;
         }
         const float inv = tot > 0.f ? 1.f / tot : 0.f;
-        // this CTA's own split comes from TMEM; the others from the
-        // partials, 32 columns (eight 16-byte loads in flight) at a time
-        float w_own = 0.f;
-#pragma unroll
-        for (int z = 0; z < kMaxSplits; ++z)
-          if (z == split) w_own = wz[z] * inv * inv_l;
 #pragma unroll 1
-        for (int c0 = 0; c0 < kDvHalf; c0 += 64) {
-          uint32_t oa[32], ob[32];
-          load_o64(c0, oa, ob);
+        for (int z = 0; z < prm.nsplit; ++z) wts[z * 128 + r] *= inv;
+        if (hv && half == 0 && prm.lse) prm.lse[(size_t)t * prm.H + h] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+        __syncwarp();
+        // the warp merges its 32 rows, four at a time; this CTA's own split
+        // is read from the stage, the others from the partials
+        const int rw = (warp & 3) * 32;  // first row of this warp
+        const float* parts = prm.o_part + orow0;
+        const size_t zstride = (size_t)prm.T * prm.H * kDv;
+#pragma unroll 1
+        for (int i0 = 0; i0 < nrows; i0 += 4) {
+          float4 acc[4][2];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            oa[j] = __float_as_uint(__uint_as_float(oa[j]) * w_own);
-            ob[j] = __float_as_uint(__uint_as_float(ob[j]) * w_own);
+          for (int u = 0; u < 4; ++u) {
+            const float w = wts[split * 128 + rw + i0 + u];
+            const float* sr = stg + (i0 + u) * kStageLd;
+            const float4 a = *reinterpret_cast<const float4*>(sr + 4 * lane);
+            const float4 b = *reinterpret_cast<const float4*>(sr + 128 + 4 * lane);
+            acc[u][0] = make_float4(a.x * w, a.y * w, a.z * w, a.w * w);
+            acc[u][1] = make_float4(b.x * w, b.y * w, b.z * w, b.w * w);
           }
 #pragma unroll 1
           for (int z = 0; z < prm.nsplit; ++z) {
             if (z == split) continue;
-            float wgt = 0.f;
+            float4 va[4][2];
 #pragma unroll
-            for (int q = 0; q < kMaxSplits; ++q)
-              if (q == z) wgt = wz[q] * inv;
-            const float4* src =
-                reinterpret_cast<const float4*>(prm.o_part + ((size_t)z * prm.T * prm.H) * kDv + orow + c0);
-            float4 v[16];
+            for (int u = 0; u < 4; ++u) {
+              const bool live = i0 + u < nrows;
+              const float4* src = reinterpret_cast<const float4*>(parts + z * zstride + (size_t)(i0 + u) * kDv);
+              va[u][0] = live ? __ldcg(src + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+              va[u][1] = live ? __ldcg(src + 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
 #pragma unroll
-            for (int u = 0; u < 16; ++u) v[u] = hv ? __ldcg(src + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int u = 0; u < 4; ++u) {
+              const float w = wts[z * 128 + rw + i0 + u];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              oa[4 * u] = __float_as_uint(fmaf(wgt, v[u].x, __uint_as_float(oa[4 * u])));
-              oa[4 * u + 1] = __float_as_uint(fmaf(wgt, v[u].y, __uint_as_float(oa[4 * u + 1])));
-              oa[4 * u + 2] = __float_as_uint(fmaf(wgt, v[u].z, __uint_as_float(oa[4 * u + 2])));
-              oa[4 * u + 3] = __float_as_uint(fmaf(wgt, v[u].w, __uint_as_float(oa[4 * u + 3])));
-              ob[4 * u] = __float_as_uint(fmaf(wgt, v[8 + u].x, __uint_as_float(ob[4 * u])));
-              ob[4 * u + 1] = __float_as_uint(fmaf(wgt, v[8 + u].y, __uint_as_float(ob[4 * u + 1])));
-              ob[4 * u + 2] = __float_as_uint(fmaf(wgt, v[8 + u].z, __uint_as_float(ob[4 * u + 2])));
-              ob[4 * u + 3] = __float_as_uint(fmaf(wgt, v[8 + u].w, __uint_as_float(ob[4 * u + 3])));
+              for (int e = 0; e < 2; ++e) {
+                acc[u][e].x = fmaf(w, va[u][e].x, acc[u][e].x);
+                acc[u][e].y = fmaf(w, va[u][e].y, acc[u][e].y);
+                acc[u][e].z = fmaf(w, va[u][e].z, acc[u][e].z);
+                acc[u][e].w = fmaf(w, va[u][e].w, acc[u][e].w);
+              }
             }
           }
-          if (hv) {
-            store_bf16_32(prm.o + orow + c0, oa, 1.f);
-            store_bf16_32(prm.o + orow + c0 + 32, ob, 1.f);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (i0 + u < nrows) {
+              uint16_t* dst = prm.o + orow0 + (size_t)(i0 + u) * kDv;
+              store_bf16_4(dst + 4 * lane, acc[u][0]);
+              store_bf16_4(dst + 128 + 4 * lane, acc[u][1]);
+            }
           }
         }
-        if (hv && half == 0 && prm.lse) prm.lse[(size_t)t * prm.H + h] = tot > 0.f ? mx + logf(tot) : -INFINITY;
       }
     }
   }
@@ -911,6 +953,7 @@ size_t attend_workspace_bytes(int T, int H, int nsplit) {
 
 int run_attend(cudaStream_t stream, AttendParams prm, void* ws, size_t ws_bytes) {
   if (prm.T == 0 || prm.H == 0) return DSA_OK;
+  if (prm.ps < kSubKeys || (prm.ps & (prm.ps - 1))) return DSA_ERR_UNSUPPORTED;  // pages: 2^n rows, n >= 5
   const int cols = 2 * ((prm.H + 127) / 128);
   if (prm.nsplit > 1) {
     if (!ws || ws_bytes < attend_workspace_bytes(prm.T, prm.H, prm.nsplit)) return DSA_ERR_WORKSPACE;
