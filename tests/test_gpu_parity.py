@@ -120,6 +120,36 @@ def test_sparse_mla_decode(dsa, case, unit_kind, H):
     np.testing.assert_allclose(l[fin], ref_l[fin], rtol=1e-4, atol=1e-4)
 
 
+@pytest.mark.parametrize("unit_kind", ["token", "page"])
+@pytest.mark.parametrize("H", [128, 40])
+def test_sparse_mla_decode_most_splits(dsa, unit_kind, H):
+    """One decode token with a long selection: the key list is split over the
+    most CTAs the kernel allows (8), and with H = 40 some head rows of the
+    merge are missing."""
+    dev = torch.device("cuda")
+    ps = 64
+    wl = DI.random_small(411 + H, [1], [4000], H=H, page_size=ps, k=64, k_pages=3)
+    rg = wl.rg
+    rng = np.random.default_rng(11)
+    unit = 1 if unit_kind == "token" else ps
+    K = 512 if unit == 1 else 16
+    sel = _rand_sel(rng, rg, K, unit, dense=True)
+    sel[0, 5:K:7] = -1  # holes inside the row
+    meta = meta_to(rg, dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    o, lse = dsa.dsa_sparse_mla_decode(wl.q[0].to(dev), wl.kv[0].to(dev), *meta, torch.from_numpy(sel).to(dev),
+                                       unit=unit, sm_scale=wl.sm_scale, want_lse=True, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    ref_o, ref_l = O.sparse_mla(f32(wl.q[0]), f32(wl.kv[0]), **meta_np(rg), sel=sel, unit=unit,
+                                sm_scale=wl.sm_scale, Dv=512)
+    check_attention(o, ref_o)
+    l = lse.cpu().numpy()
+    fin = np.isfinite(ref_l)
+    assert np.array_equal(np.isfinite(l), fin)
+    np.testing.assert_allclose(l[fin], ref_l[fin], rtol=1e-4, atol=1e-4)
+
+
 @pytest.mark.parametrize("case", ["prefill", "mixed", "tails", "extend"])
 @pytest.mark.parametrize("QB", [32, 64])
 def test_block_union_and_qblock(dsa, case, QB):
