@@ -107,3 +107,34 @@ class LayerRunner:
         """Every layer of the workload once (IndexShare across layers)."""
         for layer in range(len(self.types)):
             self.layer_step(layer)
+
+    def step_host(self, h_q_idx, h_w, h_q, h_meta, h_topk, h_o, side):
+        """One step from and to pinned host buffers (same shapes as the device
+        tensors): the indexer inputs and the metadata are copied on the
+        current stream, the attention queries (the largest input, needed only
+        by the attention) on the stream ``side`` while the indexer runs; the
+        token selections of the first full slot and every layer's output are
+        read back at the end. Can be captured in a CUDA graph."""
+        cur = torch.cuda.current_stream(self.dev)
+        side.wait_stream(cur)  # the previous step has finished reading q
+        with torch.cuda.stream(side):
+            for d, h in zip(self.q, h_q):
+                d.copy_(h, non_blocking=True)
+        self.q_idx.copy_(h_q_idx, non_blocking=True)
+        self.w.copy_(h_w, non_blocking=True)
+        for d, h in zip(self.meta, h_meta):
+            d.copy_(h, non_blocking=True)
+        joined = False
+        for layer in range(len(self.types)):
+            if self.full_slot[layer] >= 0:
+                slot = self.full_slot[layer]
+                self.index(slot)
+                if self.prefill:
+                    self.union(slot)
+            if not joined:
+                cur.wait_stream(side)
+                joined = True
+            self.attend(layer)
+        h_topk.copy_(self.topk[0], non_blocking=True)
+        for h, d in zip(h_o, self.o):
+            h.copy_(d, non_blocking=True)
