@@ -77,3 +77,136 @@ def test_selftest_wait_timeout_validates_on_host(dsa):
     assert L.dsa_selftest_wait_timeout(None, 0, fake) == -1
     assert L.dsa_selftest_wait_timeout(None, 10**11, fake) == -1
     assert L.dsa_selftest_wait_timeout(None, 1000, None) == -1
+
+
+# ---------------------------------------------------------------- host checks
+# Every case below is rejected (or, for T == 0, accepted as a no-op) before
+# the library makes any CUDA call, so the fake device pointers are never
+# dereferenced and no GPU is needed. The codes are the ones include/dsa.h
+# documents.
+OK, INVALID, UNSUPPORTED, WORKSPACE, ALIGNMENT = 0, -1, -2, -3, -7
+
+
+def _ptr(addr=4096):
+    import ctypes
+
+    return ctypes.c_void_p(addr)
+
+
+def _decode_args(**kw):
+    a = dict(stream=None, q=_ptr(), kv=_ptr(), row_stride=576, seq_lens=_ptr(), cu_q_lens=_ptr(),
+             cu_kv_lens=_ptr(), page_indices=_ptr(), sel=_ptr(), K=64, unit=1, T=4, S=4, P=16, PTW=16, ps=64,
+             H=128, Dk=576, Dv=512, sm_scale=0.1, o=_ptr(), lse=None, ws=_ptr(), ws_bytes=1 << 20,
+             dev_status=None)
+    a.update(kw)
+    return list(a.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ps=48), UNSUPPORTED),               # page sizes 32, 64, 128 only
+    (dict(row_stride=600), UNSUPPORTED),      # latent rows of 576 or 640
+    (dict(Dv=256), UNSUPPORTED),
+    (dict(Dk=512), UNSUPPORTED),
+    (dict(unit=7), INVALID),                  # unit is 1 (tokens) or ps (pages)
+    (dict(K=0), INVALID),
+    (dict(sel=None), INVALID),
+    (dict(sm_scale=float("nan")), INVALID),
+    (dict(q=_ptr(4098)), ALIGNMENT),
+    (dict(o=None), INVALID),
+    (dict(seq_lens=None), INVALID),
+    (dict(T=-1), INVALID),
+    (dict(T=0, S=0, P=0, PTW=0), OK),         # nothing to do, nothing enqueued
+])
+def test_sparse_mla_decode_host_checks(dsa, kw, code):
+    assert dsa.lib().dsa_sparse_mla_decode(*_decode_args(**kw)) == code
+
+
+def _dense_args(**kw):
+    a = dict(stream=None, q=_ptr(), kv=_ptr(), row_stride=576, seq_lens=_ptr(), cu_q_lens=_ptr(),
+             cu_kv_lens=_ptr(), page_indices=_ptr(), max_kv=1024, T=4, S=4, P=16, PTW=16, ps=64, H=128, Dk=576,
+             Dv=512, sm_scale=0.1, sliding_window=0, soft_cap=0.0, o=_ptr(), lse=None, ws=_ptr(),
+             ws_bytes=1 << 20, dev_status=None)
+    a.update(kw)
+    return list(a.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(sliding_window=-1), INVALID),
+    (dict(soft_cap=-1.0), INVALID),
+    (dict(soft_cap=float("inf")), INVALID),
+    (dict(max_kv=0), INVALID),
+    (dict(ps=100), UNSUPPORTED),
+    (dict(kv=_ptr(4100)), ALIGNMENT),
+    (dict(T=0, S=0, P=0, PTW=0), OK),
+])
+def test_dense_mla_host_checks(dsa, kw, code):
+    assert dsa.lib().dsa_dense_mla(*_dense_args(**kw)) == code
+
+
+def _write_back_args(**kw):
+    a = dict(stream=None, rows=_ptr(), src_stride=576, D=576, cache=_ptr(), cache_stride=576, seq_lens=_ptr(),
+             cu_q_lens=_ptr(), cu_kv_lens=_ptr(), page_indices=_ptr(), T=4, S=4, P=16, PTW=16, ps=64,
+             dev_status=None)
+    a.update(kw)
+    return list(a.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=100), UNSUPPORTED),               # rows move in 16-byte pieces
+    (dict(D=640, src_stride=576), UNSUPPORTED),
+    (dict(cache_stride=580), UNSUPPORTED),
+    (dict(rows=None), INVALID),
+    (dict(page_indices=None), INVALID),
+    (dict(ps=0), INVALID),
+    (dict(cache=_ptr(4104)), ALIGNMENT),
+    (dict(T=-2), INVALID),
+    (dict(T=0), OK),
+    (dict(D=0), OK),
+])
+def test_paged_write_back_host_checks(dsa, kw, code):
+    assert dsa.lib().dsa_paged_write_back(*_write_back_args(**kw)) == code
+
+
+def _pages_args(**kw):
+    a = dict(stream=None, topk=_ptr(), T=4, K=64, ps=64, max_pages=1024, cap=512, pages=_ptr(), counts=None,
+             dev_status=None)
+    a.update(kw)
+    return list(a.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cap=0), INVALID),
+    (dict(ps=0), INVALID),
+    (dict(K=-1), INVALID),
+    (dict(max_pages=0), UNSUPPORTED),
+    (dict(max_pages=(1 << 20) + 1), UNSUPPORTED),
+    (dict(pages=None), INVALID),
+    (dict(topk=None), INVALID),
+    (dict(T=0), OK),
+])
+def test_topk_pages_host_checks(dsa, kw, code):
+    assert dsa.lib().dsa_topk_pages_from_tokens(*_pages_args(**kw)) == code
+
+
+def _approx_args(**kw):
+    a = dict(stream=None, q=_ptr(), w=_ptr(), kcache=_ptr(), seq_lens=_ptr(), cu_q_lens=_ptr(), cu_kv_lens=_ptr(),
+             page_indices=_ptr(), T=4, S=4, P=16, PTW=16, ps=64, Hi=32, Di=128, max_kv=1024, k=64, over=4,
+             topk=_ptr(), ws=_ptr(), ws_bytes=1 << 30, dev_status=None)
+    a.update(kw)
+    return list(a.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(over=0), INVALID),
+    (dict(k=0), INVALID),
+    (dict(topk=None), INVALID),
+    (dict(Hi=16), UNSUPPORTED),               # 32 indexer heads of 128 dims
+    (dict(Di=64), UNSUPPORTED),
+    (dict(k=16385), UNSUPPORTED),             # the sort of the winners holds 16 K
+    (dict(ws=None), WORKSPACE),
+    (dict(ws_bytes=16), WORKSPACE),
+    (dict(w=_ptr(4108)), ALIGNMENT),
+    (dict(T=0, S=0, P=0, PTW=0), OK),
+])
+def test_indexer_topk_approx_host_checks(dsa, kw, code):
+    assert dsa.lib().dsa_indexer_topk_approx(*_approx_args(**kw)) == code
