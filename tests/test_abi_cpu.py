@@ -210,3 +210,69 @@ def _approx_args(**kw):
 ])
 def test_indexer_topk_approx_host_checks(dsa, kw, code):
     assert dsa.lib().dsa_indexer_topk_approx(*_approx_args(**kw)) == code
+
+
+def _indexer_args(**kw):
+    a = dict(stream=None, q=_ptr(), w=_ptr(), kcache=_ptr(), seq_lens=_ptr(), cu_q_lens=_ptr(), cu_kv_lens=_ptr(),
+             page_indices=_ptr(), T=4, S=4, P=16, PTW=16, ps=64, Hi=32, Di=128, max_kv=1024, k=64, topk=_ptr(),
+             topk_scores=None, ws=_ptr(), ws_bytes=1 << 30, dev_status=None)
+    a.update(kw)
+    return list(a.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(topk=None), INVALID),
+    (dict(k=0), INVALID),
+    (dict(max_kv=0), INVALID),
+    (dict(Hi=64), UNSUPPORTED),
+    (dict(ps=16), UNSUPPORTED),
+    (dict(ws=None), WORKSPACE),
+    (dict(ws_bytes=64), WORKSPACE),
+    (dict(kcache=_ptr(4112 + 4)), ALIGNMENT),
+    (dict(cu_kv_lens=None), INVALID),
+    (dict(T=0, S=0, P=0, PTW=0), OK),
+])
+def test_indexer_topk_host_checks(dsa, kw, code):
+    assert dsa.lib().dsa_indexer_topk(*_indexer_args(**kw)) == code
+
+
+def _union_args(**kw):
+    a = dict(stream=None, topk_units=_ptr(), T=64, K=4, QB=32, u_max=0, cu_q_lens=_ptr(), cu_kv_lens=_ptr(), S=2,
+             ps=64, PTW=16, units=_ptr(), member=_ptr(), counts=_ptr(), dev_status=None)
+    a.update(kw)
+    return list(a.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(QB=48), INVALID),                   # query blocks of a multiple of 32 tokens
+    (dict(QB=2048), INVALID),
+    (dict(K=0), INVALID),
+    (dict(PTW=0), INVALID),
+    (dict(cu_kv_lens=None), INVALID),
+    (dict(member=None), INVALID),
+    (dict(T=0), OK),
+])
+def test_block_union_host_checks(dsa, kw, code):
+    assert dsa.lib().dsa_build_block_union(*_union_args(**kw)) == code
+
+
+def _qblock_args(**kw):
+    a = dict(stream=None, q=_ptr(), kv=_ptr(), row_stride=576, seq_lens=_ptr(), cu_q_lens=_ptr(),
+             cu_kv_lens=_ptr(), page_indices=_ptr(), units=_ptr(), member=_ptr(), counts=_ptr(), QB=32, u_max=64,
+             T=64, S=2, P=16, PTW=16, ps=64, H=128, Dk=576, Dv=512, sm_scale=0.1, o=_ptr(), lse=None,
+             dev_status=None)
+    a.update(kw)
+    return list(a.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(QB=40), INVALID),
+    (dict(u_max=0), INVALID),
+    (dict(counts=None), INVALID),
+    (dict(sm_scale=float("inf")), INVALID),
+    (dict(row_stride=512), UNSUPPORTED),
+    (dict(o=_ptr(4120 + 2)), ALIGNMENT),
+    (dict(T=0, S=0, P=0, PTW=0), OK),
+])
+def test_prefill_qblock_host_checks(dsa, kw, code):
+    assert dsa.lib().dsa_sparse_mla_prefill_qblock(*_qblock_args(**kw)) == code
