@@ -275,7 +275,8 @@ __device__ void select_row_global(const float* __restrict__ g, int n, int k, int
   }
 }
 
-// Row staged in shared memory as ordered keys.
+// Row staged in shared memory as ordered keys; the histograms of the first
+// pass (top digit) were counted while staging.
 __device__ void select_row_staged(const float* __restrict__ g, const uint32_t* __restrict__ s_row, int n, int k,
                                   int32_t* __restrict__ out_idx, float* __restrict__ out_val, uint32_t* hist,
                                   int* s_tmp) {
@@ -284,7 +285,8 @@ __device__ void select_row_staged(const float* __restrict__ g, const uint32_t* _
   int remaining = k;
   __shared__ int s_sel[2];
   const int nround = (n + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
-  for (int pass = 0; pass < 4; ++pass) {
+  pick_digit(hist, 24, prefix, mask, remaining, s_sel);
+  for (int pass = 1; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
     for (int i = tid; i < kTopkWarps * 256; i += kTopkThreads) hist[i] = 0;
     __syncthreads();
@@ -318,7 +320,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const float* __
     return;
   }
   if (n <= cap) {
-    // stage with many independent loads in flight
+    // stage with many independent loads in flight, counting the top digit of
+    // every key on the way (the first radix pass)
+    for (int i = threadIdx.x; i < kTopkWarps * 256; i += kTopkThreads) hist[i] = 0;
+    __syncthreads();
+    uint32_t* wh = hist + warp_id() * 256;
     for (int b0 = 0; b0 < n; b0 += kTopkThreads * 8) {
       float v[8];
 #pragma unroll
@@ -329,7 +335,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const float* __
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int i = b0 + u * kTopkThreads + threadIdx.x;
-        if (i < n) s_row[i] = ordered_key(v[u]);
+        if (i < n) {
+          const uint32_t key = ordered_key(v[u]);
+          s_row[i] = key;
+          atomicAdd(wh + (key >> 24), 1u);
+        }
       }
     }
     __syncthreads();
