@@ -505,3 +505,52 @@ def test_approx_topk_selects_bin_maxima_and_count():
         bin_idx = np.arange(j % B, 5000, B)
         if x[j] == x[bin_idx].max():
             assert j in set(sel.tolist())
+
+
+# ------------------------------------------- composed entries, small helpers
+def test_hand_worked_selections_through_the_indexer_entries():
+    """The composed oracle entries (score the paged cache, then select) give
+    the hand-worked selections, with kv_len cutting the row; the cache holds
+    NaN past kv_len, so a read of a masked position would show."""
+    with open(os.path.join(GOLDEN, "indexer_hand_example.json")) as f:
+        gold = json.load(f)
+    for case in gold["cases"]:
+        q = np.array(case["q"], np.float32)[None]
+        w = np.array(case["w"], np.float32)[None]
+        keys = np.array(case["keys"], np.float32)
+        for tk in case["topk"]:
+            kv = tk["kv_len"]
+            meta = _one_seq_meta(kv, ps=2)
+            cache = _cache_from_logical(keys[:kv], 2, meta["page_indices"], len(meta["page_indices"]))
+            sel, rows = O.indexer_topk(q, w, cache, k=tk["k"], **meta)
+            assert sel[0].tolist() == tk["sel"], (case["name"], tk)
+            np.testing.assert_array_equal(rows[0], np.array(case["scores"][:kv], np.float32))
+        for pk in case["page_topk"]:
+            kv, ps = pk["kv_len"], pk["ps"]
+            meta = _one_seq_meta(kv, ps=ps)
+            cache = _cache_from_logical(keys[:kv], ps, meta["page_indices"], len(meta["page_indices"]))
+            sel, _ = O.indexer_page_topk(q, w, cache, k_pages=pk["k_pages"], **meta)
+            assert sel[0].tolist() == pk["sel"], (case["name"], pk)
+
+
+def test_score_row_worked_by_hand():
+    # two heads, three keys: dots h0 = (1, -1, 3), h1 = (2, 4, -5); relu, then
+    # weights (2, 3): 2*(1, 0, 3) + 3*(2, 4, 0) = (8, 12, 6)
+    q = np.array([[1.0, 0.0], [0.0, 1.0]], np.float32)
+    w = np.array([2.0, 3.0], np.float32)
+    keys = np.array([[1.0, 2.0], [-1.0, 4.0], [3.0, -5.0]], np.float32)
+    np.testing.assert_array_equal(O.indexer_score_row(q, w, keys), np.array([8.0, 12.0, 6.0], np.float32))
+
+
+def test_page_scores_of_row_worked_by_hand():
+    row = np.array([1.0, 5.0, 2.0, -3.0, 0.5], np.float32)
+    # pages of two: max(1, 5), max(2, -3), and the partial last page 0.5
+    np.testing.assert_array_equal(O.page_scores_of_row(row, 2), np.array([5.0, 2.0, 0.5], np.float32))
+    np.testing.assert_array_equal(O.page_scores_of_row(row, 1), row)  # page size 1: the row itself
+    np.testing.assert_array_equal(O.page_scores_of_row(row, 8), np.array([5.0], np.float32))
+
+
+def test_selected_positions_worked_by_hand():
+    assert O.selected_positions([5, -1, 2, 5], 1, 4).tolist() == [5, 2, 5]  # tokens: -1 dropped, as given
+    assert O.selected_positions([2, -1, 0], 4, 4).tolist() == [8, 9, 10, 11, 0, 1, 2, 3]  # pages of 4
+    assert O.selected_positions([-1, -1], 4, 4).tolist() == []
