@@ -29,6 +29,16 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "DSA layer tokens/s (decode, prefill) and % of HBM / tensor-core roofline"
+
+# the key lengths of each workload, as the dsa_inputs builders draw them
+KV_LEN_DESC = {
+    "tiny_decode": "1024",
+    "batched_decode": "U{4096..8192}",
+    "long_decode": "131072",
+    "single_prefill": "8192 (one request, prefix 0)",
+    "ragged_mixed": "decode U{8192..131072}; extends of 4096 on prefixes 0/16384/65536/110592",
+}
+
 L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
 
 
@@ -536,7 +546,7 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": args.workload, "requests": wl.rg.S, "tokens_per_step": T,
                        "layers": len(rn.types),
-                       "kv_len": "U{4096..8192}" if args.workload == "batched_decode" else "see DESIGN.md",
+                       "kv_len": KV_LEN_DESC.get(args.workload, "per request, from the workload"),
                        "k": wl.k, "mla_heads": wl.H, "page_size": wl.rg.page_size,
                        "l2": "flushed (512 MB write) before every timed step", "cuda_graph": graph is not None,
                        "parallelism": "replicas" if world > 1 else "single"},

@@ -19,7 +19,7 @@ exactly); the indexer score is rounded once to fp32, as the pages keep scores
 in fp32. The approximate top-k of the pages (``approx_max_k``) is replaced by
 the exact top-k, ties going to the lower index.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
   * selected sets are emitted in ascending index order, -1 padded (the pages
     emit score order; every consumer is order-invariant);
   * the attention masks every key by both ``j < kv_len`` and ``j <= pos``
