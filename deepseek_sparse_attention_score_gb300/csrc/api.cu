@@ -341,9 +341,6 @@ int dsa_sparse_mla_decode(dsa_stream_t stream, const uint16_t* q, const uint16_t
   return run_attend(static_cast<cudaStream_t>(stream), prm, ws, ws_bytes);
 }
 
-// No-allocation variant of dsa_sparse_mla_decode (declared in dsa.h): the
-// same checks and split choice; the split scratch is the library's built-in
-// device array instead of a caller workspace.
 int dsa_dense_mla(dsa_stream_t stream, const uint16_t* q, const uint16_t* kv, int row_stride, const int32_t* seq_lens,
                   const int32_t* cu_q_lens, const int32_t* cu_kv_lens, const int32_t* page_indices, int max_kv,
                   int T, int S, int P, int PTW, int ps, int H, int Dk, int Dv, float sm_scale, int sliding_window,
@@ -388,6 +385,9 @@ int dsa_dense_mla(dsa_stream_t stream, const uint16_t* q, const uint16_t* kv, in
   return run_attend(static_cast<cudaStream_t>(stream), prm, ws, ws_bytes);
 }
 
+// No-allocation variant of dsa_sparse_mla_decode: the same checks and split
+// choice; the split scratch is the library's built-in device array instead of
+// a caller workspace.
 int dsa_sparse_mla_decode_noalloc(dsa_stream_t stream, const uint16_t* q, const uint16_t* kv, int row_stride,
                                   const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
                                   const int32_t* page_indices, const int32_t* sel, int K, int unit, int T, int S,

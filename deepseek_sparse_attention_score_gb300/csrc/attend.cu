@@ -26,6 +26,8 @@
 // rows, or a query block's union + membership bitmap); runs of 32
 // consecutive rows of one page are fetched with 2-D TMA boxes, scattered
 // rows with coalesced cp.async. Masked keys are zero-filled or carry P = 0.
+#include <atomic>
+
 #include "common.cuh"
 #include "attend.cuh"
 
@@ -993,16 +995,19 @@ static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 // Device address of the array on the current device. In host code the name
 // g_static_scratch is only a host-side stand-in, so the address is resolved
 // once per device, with that device current, the first time it is needed.
+// Host threads may race to resolve it: each gets the same address, and the
+// atomic slots keep the race benign. Devices 0..kMaxScratchDevices-1 only.
+constexpr int kMaxScratchDevices = 64;
 static void* static_scratch_address() {
-  static void* addr[64] = {};
+  static std::atomic<void*> addr[kMaxScratchDevices];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return nullptr;
-    addr[dev] = p;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) return nullptr;
+  void* cur = addr[dev].load(std::memory_order_acquire);
+  if (!cur) {
+    if (cudaGetSymbolAddress(&cur, g_static_scratch) != cudaSuccess) return nullptr;
+    addr[dev].store(cur, std::memory_order_release);
   }
-  return addr[dev];
+  return cur;
 }
 
 int run_attend_static_scratch(cudaStream_t stream, AttendParams prm) {

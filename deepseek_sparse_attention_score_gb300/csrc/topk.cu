@@ -242,7 +242,11 @@ __device__ void select_row_global(const float* __restrict__ g, int n, int k, int
       }
       gbase = __shfl_sync(0xffffffffu, gbase, 0);
       ebase = __shfl_sync(0xffffffffu, ebase, 0);
-      if (is_gt) gt_list[gbase + __popc(gb & lt)] = i;
+      if (is_gt) {
+        // a selection larger than the list is emitted in order below instead
+        const int pos = gbase + __popc(gb & lt);
+        if (pos < list_cap) gt_list[pos] = i;
+      }
       if (is_eq) {
         const int pos = ebase + __popc(eb & lt);
         if (pos < list_cap) eq_list[pos] = i;
@@ -252,7 +256,8 @@ __device__ void select_row_global(const float* __restrict__ g, int n, int k, int
   __syncthreads();
   const int neq = s_cnt[1];
   if (neq > list_cap || k > list_cap) {
-    // too many ties to collect: ordered emission straight from global memory
+    // too many winners or ties to collect (the lists stopped at list_cap
+    // entries): ordered emission straight from global memory
     emit_ordered<false>(g, nullptr, n, kstar, need_eq, out_idx, out_val, s_tmp);
     return;
   }

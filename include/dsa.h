@@ -204,7 +204,8 @@ DSA_API int dsa_sparse_mla_decode(dsa_stream_t stream, const uint16_t* q, const 
  *    serialise them.
  *  - Limit: a problem whose split scratch would exceed 24 MiB returns
  *    DSA_ERR_SCRATCH_LIMIT and enqueues nothing; use dsa_sparse_mla_decode
- *    with a workspace for it.
+ *    with a workspace for it. Only devices 0..63 are served: on a device
+ *    with a higher ordinal a call that needs the array returns DSA_ERR_CUDA.
  * ------------------------------------------------------------------------ */
 DSA_API int dsa_sparse_mla_decode_noalloc(dsa_stream_t stream, const uint16_t* q, const uint16_t* kv,
                                           int row_stride, const int32_t* seq_lens, const int32_t* cu_q_lens,

@@ -1,467 +1,403 @@
-"""CPU oracle for the DSA sparse-attention hot path (test infrastructure only).
+"""Python binding of the C++ CPU oracle (``oracle/dsa_oracle.cpp``).
 
-This is the plain, slow, obviously correct definition of every step of the
-path, written from the sglang-jax DSA pages:
+TEST INFRASTRUCTURE ONLY: ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference leg of ``bench.py`` may import this module. It shares
+no code with the CUDA library and imports nothing from it.
 
-  * "ref.py" (jnp reference implementations): ``build_index_share_map``,
-    ``streamindex_topk_ref``, ``streamindex_page_topk_ref``, ``sparse_mla_ref``;
-  * "sparse_mla_prefill_qblock.py" (blocked sparse-MLA prefill):
-    ``build_block_unit_tables``, ``_qblock_kernel``,
-    ``sparse_mla_attention_qblock``, ``prefill_write_and_attend_ragged_qblock``;
-  * "dsa_sparse_backend.py" (DSA sparse attention backend): the IndexShare
-    dispatch, the page budget of the prefill page top-k, and the paged cache
-    write of the new tokens (``_scatter_paged``) that precedes the path.
+Every step of the method is computed in ``dsa_oracle.cpp`` (plain C++17, fp64,
+OpenMP over query rows; see its header for the pages it follows and the
+readings it takes). This module only marshals arguments: it picks the rows of
+the requested tokens, passes arrays in their own element type (fp32, fp64 or
+bf16 bit patterns, all widened exactly by the C++ side) and shapes the
+results. Queries, weights and selections may be given as arrays indexed by
+token or as any mapping token -> row, so large batches can be checked on a
+sample of rows; caches are arrays.
 
-Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
-leg may import this module. It shares no code with the CUDA library and
-imports nothing from it. Floating point is fp64 (bf16 inputs are widened
-exactly); the indexer score is rounded once to fp32, as the pages keep scores
-in fp32. The approximate top-k of the pages (``approx_max_k``) is replaced by
-the exact top-k, ties going to the lower index.
-
-Readings taken where the pages are silent:
-  * selected sets are emitted in ascending index order, -1 padded (the pages
-    emit score order; every consumer is order-invariant);
-  * the attention masks every key by both ``j < kv_len`` and ``j <= pos``
-    (the jnp reference applies only the first, the qblock kernel both; they
-    coincide on indices produced by the indexer);
-  * a row with no valid key outputs 0 (the pages' masked softmax does the same).
-
-Queries may be given as arrays or as any mapping token -> row (so large
-batches can be checked on a sample of rows); caches are arrays.
-
-Every function here is pinned by ``tests/test_oracle_pins.py`` against values
-and properties fixed outside this file (hand-worked examples, brute force on
-tiny inputs, closed forms, reductions to library routines); none is
-"parity unpinned".
+The shared library is compiled from source on first use (``g++ -fopenmp``),
+by ``build_oracle.build()``.
 """
 from __future__ import annotations
 
+import ctypes
+from collections.abc import Mapping
+
 import numpy as np
+
+from . import build_oracle
 
 NEG_INF = float("-inf")
 
+_F32, _F64, _BF16 = 0, 1, 2
+_P = ctypes.c_void_p
+_L = ctypes.c_longlong
+_D = ctypes.c_double
+_lib = None
 
-# ---------------------------------------------------------------------------
-# input widening and ragged metadata
-# ---------------------------------------------------------------------------
 
+def _load():
+    global _lib
+    if _lib is None:
+        L = ctypes.CDLL(build_oracle.build())
+        sig = {
+            "orc_num_threads": ([], ctypes.c_int),
+            "orc_widen": ([_P, ctypes.c_int, _L, _P], None),
+            "orc_token_seq": ([_P, _L, _L, _P], None),
+            "orc_token_geometry": ([_P, _P, _L, _L, _P, _P, _P], None),
+            "orc_physical_rows": ([_P, _P, _L, _L, _P, _L, _P], None),
+            "orc_share_map": ([_P, _L, _L, _P, _P, _P], ctypes.c_int),
+            "orc_score_row": ([_P, ctypes.c_int, _P, ctypes.c_int, _P, ctypes.c_int, _L, _L, _L, _P], None),
+            "orc_indexer_scores": ([_P, ctypes.c_int, _P, ctypes.c_int, _P, ctypes.c_int, _L, _L, _L, _P, _P, _P,
+                                    _P, _L, _P, _L, _L, _P, _P], None),
+            "orc_topk_rows": ([_P, _L, _P, _L, _L, _P], None),
+            "orc_page_topk_rows": ([_P, _L, _P, _L, _L, _L, _P], None),
+            "orc_page_scores_row": ([_P, _L, _L, _P], None),
+            "orc_lift_units": ([_P, _L, _L, _P, _L, _P, _L, _P], None),
+            "orc_block_union": ([_P, _L, _L, _L, _L, _P, _P, _P], None),
+            "orc_selected_positions": ([_P, _L, _L, _P], _L),
+            "orc_sparse_mla": ([_P, ctypes.c_int, _P, ctypes.c_int, _L, _L, _L, _L, _L, _P, _P, _P, _P, _L, _P, _L,
+                                _P, _L, _L, _D, _P, _P], None),
+            "orc_qblock_attend": ([_P, ctypes.c_int, _P, ctypes.c_int, _L, _L, _L, _L, _L, _P, _P, _P, _P, _L, _P,
+                                   _L, _P, _P, _P, _L, _L, _D, _P, _P], None),
+            "orc_dense_mla": ([_P, ctypes.c_int, _P, ctypes.c_int, _L, _L, _L, _L, _L, _P, _P, _P, _P, _L, _P, _L,
+                               _D, _L, _D, _P], None),
+            "orc_paged_write_back": ([_P, _L, _L, _L, _P, _L, _P, _P, _P, _P, _L, _L], None),
+            "orc_topk_pages_of_tokens": ([_P, _L, _L, _L, _P], _L),
+            "orc_approx_topk_row": ([_P, _L, _L, _L, _P], None),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def num_threads() -> int:
+    """Host threads the oracle's row loops run on (OpenMP)."""
+    return int(_load().orc_num_threads())
+
+
+# ---------------------------------------------------------------- marshalling
+def _p(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _i64(x):
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int64))
+
+
+def _f32(x):
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+
+
+def _typed(x):
+    """(contiguous array, element-type code) with no rounding: fp32 and fp64
+    pass as they are, int16/uint16 are bf16 bit patterns, anything else is
+    converted to fp64."""
+    a = np.asarray(x)
+    if a.dtype == np.float32:
+        return np.ascontiguousarray(a), _F32
+    if a.dtype == np.float64:
+        return np.ascontiguousarray(a), _F64
+    if a.dtype in (np.uint16, np.int16):
+        return np.ascontiguousarray(a.view(np.uint16)), _BF16
+    return np.ascontiguousarray(a.astype(np.float64)), _F64
+
+
+def _rows(x, tokens):
+    """The rows of ``tokens`` from an array indexed by token or a mapping."""
+    if isinstance(x, Mapping):
+        return np.stack([np.asarray(x[int(t)]) for t in tokens])
+    a = np.asarray(x)
+    if len(tokens) == a.shape[0] and np.array_equal(tokens, np.arange(a.shape[0])):
+        return a
+    return a[np.asarray(tokens, dtype=np.int64)]
+
+
+def _meta(seq_lens, cu_q_lens, cu_kv_lens, page_indices):
+    return _i64(seq_lens), _i64(cu_q_lens), _i64(cu_kv_lens), _i64(page_indices)
+
+
+def _tokens(tokens, cu_q_lens):
+    if tokens is None:
+        return np.arange(int(np.asarray(cu_q_lens)[-1]), dtype=np.int64)
+    return _i64(list(tokens))
+
+
+# ---------------------------------------------------- widening and metadata
 def widen(x) -> np.ndarray:
-    """Exact fp64 view of a tensor given as bf16 bit patterns (uint16/int16)
+    """Exact fp64 values of a tensor given as bf16 bit patterns (uint16/int16)
     or as an fp32/fp64 array."""
-    x = np.asarray(x)
-    if x.dtype in (np.uint16, np.int16):
-        return (x.view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    return x.astype(np.float64)
+    a, dt = _typed(x)
+    out = np.empty(a.shape, np.float64)
+    _load().orc_widen(_p(a), dt, a.size, _p(out))
+    return out
+
+
+def _geometry(seq_lens, cu_q_lens):
+    sl, cu = _i64(seq_lens), _i64(cu_q_lens)
+    T = int(cu[-1])
+    seq, pos, nvis = (np.empty(T, np.int64) for _ in range(3))
+    _load().orc_token_geometry(_p(sl), _p(cu), len(cu) - 1, T, _p(seq), _p(pos), _p(nvis))
+    return seq, pos, nvis
 
 
 def token_seq(cu_q_lens, T=None) -> np.ndarray:
     """Request of each query token: the ``s`` with
-    ``cu_q_lens[s] <= t < cu_q_lens[s+1]`` (the searchsorted over
-    ``cu_q_lens[1:]`` with side="right" of prefill_write_and_attend_ragged_qblock)."""
-    cu = np.asarray(cu_q_lens, dtype=np.int64)
-    if T is None:
-        T = int(cu[-1])
-    t = np.arange(T, dtype=np.int64)
-    return np.searchsorted(cu[1:], t, side="right").astype(np.int64)
+    ``cu_q_lens[s] <= t < cu_q_lens[s+1]``."""
+    cu = _i64(cu_q_lens)
+    T = int(cu[-1]) if T is None else int(T)
+    seq = np.empty(T, np.int64)
+    _load().orc_token_seq(_p(cu), len(cu) - 1, T, _p(seq))
+    return seq
 
 
 def token_pos(seq_lens, cu_q_lens) -> np.ndarray:
-    """Absolute position of each query token,
-    ``abs_q = kv_len - (q_end - q_start) + (t - q_start)`` (ref.py,
-    streamindex_topk_ref, general path)."""
-    sl = np.asarray(seq_lens, dtype=np.int64)
-    cu = np.asarray(cu_q_lens, dtype=np.int64)
-    s = token_seq(cu)
-    t = np.arange(int(cu[-1]), dtype=np.int64)
-    return sl[s] - (cu[s + 1] - cu[s]) + (t - cu[s])
+    """Absolute position of each query token."""
+    return _geometry(seq_lens, cu_q_lens)[1]
 
 
 def visible_len(seq_lens, cu_q_lens) -> np.ndarray:
-    """Number of key positions token t may see: ``j < kv_len`` and ``j <= abs_q``
-    (the mask of streamindex_topk_ref). The visible set is always the prefix
-    ``[0, n)`` with ``n = clip(min(kv_len, abs_q + 1), 0)``."""
-    sl = np.asarray(seq_lens, dtype=np.int64)
-    s = token_seq(cu_q_lens)
-    pos = token_pos(seq_lens, cu_q_lens)
-    return np.clip(np.minimum(sl[s], pos + 1), 0, None)
+    """Visible prefix length of each token (``j < kv_len`` and ``j <= pos``)."""
+    return _geometry(seq_lens, cu_q_lens)[2]
 
 
 def physical_rows(cu_kv_lens, page_indices, ps, s, positions) -> np.ndarray:
-    """Flat row ``page*ps + offset`` of sequence-local key positions: request
-    ``s`` owns the packed page-table entries starting at ``cu_kv_lens[s]//ps``
-    (ref.py, ``seq_pages = page_indices[cu_kv_lens[s]//ps : ...]``)."""
-    positions = np.asarray(positions, dtype=np.int64)
-    base = int(cu_kv_lens[s]) // ps
-    pages = np.asarray(page_indices, dtype=np.int64)[base + positions // ps]
-    return pages * ps + positions % ps
+    """Flat rows ``page*ps + offset`` of sequence-local key positions."""
+    cu, pi, pos = _i64(cu_kv_lens), _i64(page_indices), _i64(positions).reshape(-1)
+    out = np.empty(len(pos), np.int64)
+    _load().orc_physical_rows(_p(cu), _p(pi), int(ps), int(s), _p(pos), len(pos), _p(out))
+    return out
 
 
-# ---------------------------------------------------------------------------
-# a7: IndexShare layer -> slot map
-# ---------------------------------------------------------------------------
-
+# ---------------------------------------------------------------- a7
 class ShareMapError(ValueError):
     pass
 
 
 def build_index_share_map(indexer_types, skip_offset, num_layers):
-    """ref.py, ``build_index_share_map``: a "full" layer opens a new slot, a
-    "shared" layer consumes the nearest preceding full layer's slot; a shared
-    layer with no preceding full layer, or an unknown type, is an error.
-    ``None`` means every layer is full. ``skip_offset`` is accepted and, as on
-    the page, not used."""
+    """ref.py, build_index_share_map: returns (full_slot {layer: slot},
+    src_slot {layer: slot}, number of full layers)."""
     del skip_offset
-    if indexer_types is None:
-        indexer_types = ["full"] * num_layers
-    if len(indexer_types) != num_layers:
+    codes = {"full": 0, "shared": 1}
+    types = None if indexer_types is None else np.array([codes.get(k, 2) for k in indexer_types], np.int32)
+    full = np.empty(max(1, num_layers), np.int64)
+    src = np.empty(max(1, num_layers), np.int64)
+    nfull = np.zeros(1, np.int64)
+    rc = _load().orc_share_map(None if types is None else _p(types), 0 if types is None else len(types),
+                               int(num_layers), _p(full), _p(src), _p(nfull))
+    if rc == 1:
         raise ShareMapError("indexer_types length != num_layers")
-    full_slot, src_slot = {}, {}
-    last = -1
-    for layer, kind in enumerate(indexer_types):
-        if kind == "full":
-            last = len(full_slot)
-            full_slot[layer] = last
-            src_slot[layer] = last
-        elif kind == "shared":
-            if last < 0:
-                raise ShareMapError(f"layer {layer} is shared but no preceding full layer")
-            src_slot[layer] = last
-        else:
-            raise ShareMapError(f"unknown indexer type {kind!r} at layer {layer}")
-    return full_slot, src_slot, len(full_slot)
+    if rc == 2:
+        raise ShareMapError("a shared layer has no preceding full layer")
+    if rc == 3:
+        raise ShareMapError("unknown indexer type")
+    full_slot = {l: int(full[l]) for l in range(num_layers) if full[l] >= 0}
+    src_slot = {l: int(src[l]) for l in range(num_layers)}
+    return full_slot, src_slot, int(nfull[0])
 
 
-# ---------------------------------------------------------------------------
-# a1: lightning-indexer score
-# ---------------------------------------------------------------------------
-
+# ---------------------------------------------------------------- a1 - a3
 def indexer_score_row(q_t, w_t, keys) -> np.ndarray:
-    """Score of one query token against the rows of ``keys`` ([n, D]):
-    ``s_j = sum_h relu(q[h,:] . k_j) * w[h]`` (ref.py, streamindex_topk_ref:
-    an einsum over D, relu, an einsum with the head weights). Accumulated in
-    fp64 and rounded once to fp32. No extra scale factor: the pages' score has
-    none."""
-    q_t = widen(q_t)  # [H, D]
-    w_t = widen(w_t)  # [H]
-    keys = widen(keys)  # [n, D]
-    dots = q_t @ keys.T  # [H, n]
-    s = (np.maximum(dots, 0.0) * w_t[:, None]).sum(axis=0)
-    return s.astype(np.float32)
-
-
-def indexer_scores(q, w, kcache, seq_lens, cu_q_lens, cu_kv_lens, page_indices, tokens=None):
-    """Score rows for the given tokens (all by default). Row ``t`` holds the
-    scores of the visible prefix ``[0, visible_len[t])``; every other position
-    is masked (-inf) and so is simply absent from the row."""
-    kc = np.asarray(kcache)
-    P, ps, D = kc.shape
-    flat = kc.reshape(P * ps, D)
-    seq = token_seq(cu_q_lens)
-    nvis = visible_len(seq_lens, cu_q_lens)
-    if tokens is None:
-        tokens = range(len(seq))
-    rows = []
-    for t in tokens:
-        n = int(nvis[t])
-        r = physical_rows(cu_kv_lens, page_indices, ps, int(seq[t]), np.arange(n))
-        rows.append(indexer_score_row(q[t], w[t], flat[r]) if n else np.zeros(0, np.float32))
-    return rows
-
-
-# ---------------------------------------------------------------------------
-# a2 / a3: exact top-k over tokens and over max-pooled pages
-# ---------------------------------------------------------------------------
-
-def topk_of_row(scores, k) -> np.ndarray:
-    """Exact top-k of one row: order the finite entries by (score desc, index
-    asc), keep ``min(k, n)`` of them, emit them in ascending index order, pad
-    with -1 (streamindex_topk_ref with exact selection; masked entries are
-    never selected)."""
-    scores = np.asarray(scores, dtype=np.float32)
-    idx = np.nonzero(np.isfinite(scores))[0]
-    order = np.lexsort((idx, -scores[idx].astype(np.float64)))
-    chosen = np.sort(idx[order[: min(k, len(idx))]])
-    out = np.full(k, -1, dtype=np.int32)
-    out[: len(chosen)] = chosen
+    """Scores of one query ([H, D], weights [H]) against ``keys`` [n, D]."""
+    q, qd = _typed(q_t)
+    w, wd = _typed(w_t)
+    k, kd = _typed(keys)
+    H, D = q.shape
+    n = k.shape[0]
+    out = np.empty(n, np.float32)
+    _load().orc_score_row(_p(q), qd, _p(w), wd, _p(k), kd, H, D, n, _p(out))
     return out
 
 
+def _score_matrix(q, w, kcache, seq_lens, cu_q_lens, cu_kv_lens, page_indices, tokens):
+    toks = _tokens(tokens, cu_q_lens)
+    meta = _meta(seq_lens, cu_q_lens, cu_kv_lens, page_indices)
+    kc, kd = _typed(kcache)
+    P, ps, D = kc.shape
+    if len(toks) == 0:
+        return np.zeros((0, 1), np.float32), np.zeros(0, np.int64), toks, ps
+    qr, qd = _typed(_rows(q, toks))
+    wr, wd = _typed(_rows(w, toks))
+    H = qr.shape[1]
+    nvis = _geometry(meta[0], meta[1])[2][toks]
+    ld = max(1, int(nvis.max()))
+    out = np.full((len(toks), ld), np.nan, np.float32)
+    lens = np.empty(len(toks), np.int64)
+    _load().orc_indexer_scores(_p(qr), qd, _p(wr), wd, _p(kc), kd, ps, H, D, *map(_p, meta), len(meta[1]) - 1,
+                               _p(toks), len(toks), ld, _p(out), _p(lens))
+    return out, lens, toks, ps
+
+
+def indexer_scores(q, w, kcache, seq_lens, cu_q_lens, cu_kv_lens, page_indices, tokens=None):
+    """Score rows for the given tokens (all by default): row ``t`` holds the
+    scores of its visible prefix; masked positions are absent."""
+    out, lens, _, _ = _score_matrix(q, w, kcache, seq_lens, cu_q_lens, cu_kv_lens, page_indices, tokens)
+    return [out[i, : lens[i]] for i in range(len(lens))]
+
+
+def topk_of_row(scores, k) -> np.ndarray:
+    """Exact top-k of one row (finite entries by (score desc, index asc),
+    ``min(k, n)`` of them, ascending, -1 padded)."""
+    s = _f32(scores)
+    out = np.empty((1, k), np.int64)
+    _load().orc_topk_rows(_p(s), max(1, len(s)), _p(_i64([len(s)])), 1, k, _p(out))
+    return out[0].astype(np.int32)
+
+
 def page_scores_of_row(scores, ps) -> np.ndarray:
-    """Max-pool a token score row per page of ``ps`` positions
-    (streamindex_page_topk_ref: ``scores.reshape(.., pages, ps).max(-1)``);
-    only visible positions enter the max, so every page of the visible prefix
-    has a finite score."""
-    scores = np.asarray(scores, dtype=np.float32)
-    n = len(scores)
-    npg = (n + ps - 1) // ps
-    pad = np.full(npg * ps, -np.inf, dtype=np.float32)
-    pad[:n] = scores
-    return pad.reshape(npg, ps).max(axis=1)
+    """Max-pool of one score row per page of ``ps`` positions."""
+    s = _f32(scores)
+    out = np.empty(-(-len(s) // ps), np.float32)
+    _load().orc_page_scores_row(_p(s), len(s), int(ps), _p(out))
+    return out
 
 
 def page_topk_of_row(scores, ps, k_pages) -> np.ndarray:
-    """streamindex_page_topk_ref: top ``k_pages`` pages by max-pooled score,
-    pages with score -inf dropped, sequence-local page ids (exact, ties to the
-    lower page, ascending output, -1 padded)."""
-    return topk_of_row(page_scores_of_row(scores, ps), k_pages)
+    """Top ``k_pages`` pages of one row by max-pooled score."""
+    s = _f32(scores)
+    out = np.empty((1, k_pages), np.int64)
+    _load().orc_page_topk_rows(_p(s), max(1, len(s)), _p(_i64([len(s)])), 1, int(ps), k_pages, _p(out))
+    return out[0].astype(np.int32)
 
 
 def indexer_topk(q, w, kcache, seq_lens, cu_q_lens, cu_kv_lens, page_indices, k, tokens=None):
-    rows = indexer_scores(q, w, kcache, seq_lens, cu_q_lens, cu_kv_lens, page_indices, tokens)
-    return np.stack([topk_of_row(r, k) for r in rows]) if rows else np.zeros((0, k), np.int32), rows
+    """(token top-k [n, k] int32, score rows) of the given tokens."""
+    out, lens, toks, _ = _score_matrix(q, w, kcache, seq_lens, cu_q_lens, cu_kv_lens, page_indices, tokens)
+    sel = np.empty((len(toks), k), np.int64)
+    if len(toks):
+        _load().orc_topk_rows(_p(out), out.shape[1], _p(lens), len(toks), k, _p(sel))
+    return sel.astype(np.int32), [out[i, : lens[i]] for i in range(len(lens))]
 
 
-def indexer_page_topk(q, w, kcache, seq_lens, cu_q_lens, cu_kv_lens, page_indices, k_pages,
-                      tokens=None):
-    kc = np.asarray(kcache)
-    ps = kc.shape[1]
-    rows = indexer_scores(q, w, kcache, seq_lens, cu_q_lens, cu_kv_lens, page_indices, tokens)
-    out = [page_topk_of_row(r, ps, k_pages) for r in rows]
-    return (np.stack(out) if out else np.zeros((0, k_pages), np.int32)), rows
+def indexer_page_topk(q, w, kcache, seq_lens, cu_q_lens, cu_kv_lens, page_indices, k_pages, tokens=None):
+    """(page top-k [n, k_pages] int32, score rows) of the given tokens."""
+    out, lens, toks, ps = _score_matrix(q, w, kcache, seq_lens, cu_q_lens, cu_kv_lens, page_indices, tokens)
+    sel = np.empty((len(toks), k_pages), np.int64)
+    if len(toks):
+        _load().orc_page_topk_rows(_p(out), out.shape[1], _p(lens), len(toks), ps, k_pages, _p(sel))
+    return sel.astype(np.int32), [out[i, : lens[i]] for i in range(len(lens))]
 
 
-# ---------------------------------------------------------------------------
-# a4: per-query-block union and membership
-# ---------------------------------------------------------------------------
-
+# ---------------------------------------------------------------- a4
 def lift_units(topk_units, cu_q_lens, cu_kv_lens, ps) -> np.ndarray:
-    """Lift sequence-local page ids to global page-table keys,
-    ``g = cu_kv_lens[seq(t)]//ps + p`` for ``p >= 0``, else -1
-    (sparse_mla_attention_qblock, ragged mode)."""
-    tk = np.asarray(topk_units, dtype=np.int64)
-    seq = token_seq(cu_q_lens, tk.shape[0])
-    base = np.asarray(cu_kv_lens, dtype=np.int64)[seq] // ps
-    return np.where(tk >= 0, tk + base[:, None], -1)
+    """Sequence-local page ids -> global page-table keys (-1 stays -1)."""
+    tk = _i64(topk_units)
+    cu_q = _i64(cu_q_lens)
+    out = np.empty(tk.shape, np.int64)
+    _load().orc_lift_units(_p(tk), tk.shape[0], tk.shape[1], _p(cu_q), len(cu_q) - 1, _p(_i64(cu_kv_lens)),
+                           int(ps), _p(out))
+    return out
 
 
 def block_union(units_global, QB, u_max):
-    """build_block_unit_tables: pad T to a multiple of QB with -1 rows; per
-    block the ascending unique list of the selected ids (kept up to
-    ``u_max``, -1 padded), the true (uncapped) union size, and the membership
-    ``member[b, q, u] = 1`` iff query q of block b selected ``units[b, u]``."""
-    g = np.asarray(units_global, dtype=np.int64)
+    """build_block_unit_tables: (units [nQB, u_max] int32, member
+    [nQB, QB, u_max] int8, counts [nQB] int32)."""
+    g = _i64(units_global)
     T, K = g.shape
     nqb = -(-T // QB) if T else 0
-    units = np.full((nqb, u_max), -1, dtype=np.int32)
-    member = np.zeros((nqb, QB, u_max), dtype=np.int8)
-    counts = np.zeros(nqb, dtype=np.int32)
-    for b in range(nqb):
-        blk = g[b * QB: min(T, (b + 1) * QB)]
-        uniq = np.unique(blk[blk >= 0])
-        counts[b] = len(uniq)
-        kept = uniq[:u_max]
-        units[b, : len(kept)] = kept
-        for q in range(blk.shape[0]):
-            sel = blk[q][blk[q] >= 0]
-            member[b, q, : len(kept)] = np.isin(kept, sel)
+    units = np.empty((nqb, u_max), np.int32)
+    member = np.empty((nqb, QB, u_max), np.int8)
+    counts = np.empty(nqb, np.int32)
+    if nqb:
+        _load().orc_block_union(_p(g), T, K, QB, u_max, _p(units), _p(member), _p(counts))
     return units, member, counts
 
 
-# ---------------------------------------------------------------------------
-# a5 / a6: absorbed-MLA sparse attention
-# ---------------------------------------------------------------------------
-
-def _masked_softmax_attend(q_t, keys, vals, sm_scale):
-    """fp64 masked-softmax attention of one token over the given (already
-    filtered) keys. Returns (o [H, Dv], lse [H]); no key gives o = 0 and
-    lse = -inf (sparse_mla_ref: ``p = where(valid, softmax, 0)``)."""
-    H = q_t.shape[0]
-    if keys.shape[0] == 0:
-        return np.zeros((H, vals.shape[1])), np.full(H, NEG_INF)
-    logits = sm_scale * (q_t @ keys.T)  # [H, n]
-    m = logits.max(axis=1, keepdims=True)
-    e = np.exp(logits - m)
-    l = e.sum(axis=1, keepdims=True)
-    o = (e @ vals) / l
-    return o, (m + np.log(l))[:, 0]
+# ---------------------------------------------------------------- a5 / a6
+def selected_positions(sel_row, unit, ps) -> np.ndarray:
+    """Key positions named by one selection row (tokens, or whole pages)."""
+    del ps
+    sel = _i64(sel_row).reshape(-1)
+    out = np.empty(max(1, len(sel) * unit), np.int64)
+    n = _load().orc_selected_positions(_p(sel), len(sel), int(unit), _p(out))
+    return out[:n]
 
 
-def selected_positions(sel_row, unit, ps):
-    """Key positions named by one selection row: token ids (``unit == 1``) or
-    whole pages expanded to ``p*ps .. p*ps+ps-1`` (``unit == ps``). -1 entries
-    are ignored; duplicates are kept as given."""
-    sel = np.asarray(sel_row, dtype=np.int64)
-    sel = sel[sel >= 0]
-    if unit == 1:
-        return sel
-    return (sel[:, None] * unit + np.arange(unit)[None, :]).reshape(-1)
+def _attend_inputs(q, kv, toks):
+    qr, qd = _typed(_rows(q, toks))
+    kvc, kvd = _typed(kv)
+    P, ps, W = kvc.shape
+    return qr, qd, kvc, kvd, ps, W
 
 
-def sparse_mla(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, sel, unit, sm_scale, Dv,
-               tokens=None):
-    """sparse_mla_ref: for each token, masked softmax of
-    ``sm_scale * q[t,h,:] . kv[j,:Dk]`` over the selected positions j with
-    ``0 <= j < kv_len`` and ``j <= pos(t)``, output ``sum_j p_j kv[j, :Dv]``.
-    Returns fp64 ``o [n, H, Dv]`` and ``lse [n, H]``."""
-    kvc = np.asarray(kv)
-    P, ps, Dk_row = kvc.shape
-    flat = kvc.reshape(P * ps, Dk_row)
-    seq = token_seq(cu_q_lens)
-    nvis = visible_len(seq_lens, cu_q_lens)
-    if tokens is None:
-        tokens = range(len(seq))
-    os_, ls = [], []
-    for t in tokens:
-        j = selected_positions(sel[t], unit, ps)
-        j = j[(j >= 0) & (j < nvis[t])]
-        rows = widen(flat[physical_rows(cu_kv_lens, page_indices, ps, int(seq[t]), j)])
-        qt = widen(q[t])
-        Dk = qt.shape[-1]
-        o, l = _masked_softmax_attend(qt, rows[:, :Dk], rows[:, :Dv], sm_scale)
-        os_.append(o)
-        ls.append(l)
-    return np.stack(os_), np.stack(ls)
+def sparse_mla(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, sel, unit, sm_scale, Dv, tokens=None):
+    """sparse_mla_ref over the selections: fp64 ``o [n, H, Dv]``, ``lse [n, H]``."""
+    toks = _tokens(tokens, cu_q_lens)
+    meta = _meta(seq_lens, cu_q_lens, cu_kv_lens, page_indices)
+    qr, qd, kvc, kvd, ps, W = _attend_inputs(q, kv, toks)
+    H, Dk = qr.shape[1], qr.shape[2]
+    sr = _i64(_rows(sel, toks)).reshape(len(toks), -1)
+    o = np.empty((len(toks), H, Dv), np.float64)
+    lse = np.empty((len(toks), H), np.float64)
+    if len(toks):
+        _load().orc_sparse_mla(_p(qr), qd, _p(kvc), kvd, ps, W, H, Dk, Dv, *map(_p, meta), len(meta[1]) - 1,
+                               _p(toks), len(toks), _p(sr), sr.shape[1], int(unit), float(sm_scale), _p(o), _p(lse))
+    return o, lse
 
 
-def qblock_attend(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, units, member, counts,
-                  QB, sm_scale, Dv, tokens=None):
-    """_qblock_kernel semantics: query t of block b walks the block's union
-    slots ``u < min(count, u_max)`` in order; unit ``g = units[b,u]`` covers
-    physical page ``page_indices[g]`` whose row r is key position
-    ``kp = g*ps + r - base_tok(t)``; the key is visible iff
-    ``member[b,q,u]`` and ``kp <= pos(t)`` and ``kp < kv_len(t)``. Masked
-    softmax over the visible keys; a row with none outputs 0."""
-    kvc = np.asarray(kv)
-    P, ps, Dk_row = kvc.shape
-    flat = kvc.reshape(P * ps, Dk_row)
-    seq = token_seq(cu_q_lens)
-    pos = token_pos(seq_lens, cu_q_lens)
-    sl = np.asarray(seq_lens, dtype=np.int64)
-    pi = np.asarray(page_indices, dtype=np.int64)
-    u_max = units.shape[1]
-    if tokens is None:
-        tokens = range(len(seq))
-    os_, ls = [], []
-    for t in tokens:
-        b, qq = divmod(int(t), QB)
-        s = int(seq[t])
-        base_tok = (int(cu_kv_lens[s]) // ps) * ps
-        rows_sel = []
-        for u in range(min(int(counts[b]), u_max)):
-            if not member[b, qq, u]:
-                continue
-            g = int(units[b, u])
-            kp = g * ps + np.arange(ps) - base_tok
-            ok = (kp <= pos[t]) & (kp < sl[s])
-            rows_sel.append((pi[g] * ps + np.arange(ps))[ok])
-        r = np.concatenate(rows_sel) if rows_sel else np.zeros(0, np.int64)
-        rows = widen(flat[r])
-        qt = widen(q[t])
-        Dk = qt.shape[-1]
-        o, l = _masked_softmax_attend(qt, rows[:, :Dk], rows[:, :Dv], sm_scale)
-        os_.append(o)
-        ls.append(l)
-    return np.stack(os_), np.stack(ls)
+def qblock_attend(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, units, member, counts, QB, sm_scale, Dv,
+                  tokens=None):
+    """_qblock_kernel semantics over the block unions: fp64 ``o``, ``lse``."""
+    toks = _tokens(tokens, cu_q_lens)
+    meta = _meta(seq_lens, cu_q_lens, cu_kv_lens, page_indices)
+    qr, qd, kvc, kvd, ps, W = _attend_inputs(q, kv, toks)
+    H, Dk = qr.shape[1], qr.shape[2]
+    un = _i64(units)
+    mem = np.ascontiguousarray(np.asarray(member, dtype=np.int8))
+    cnt = _i64(counts)
+    o = np.empty((len(toks), H, Dv), np.float64)
+    lse = np.empty((len(toks), H), np.float64)
+    if len(toks):
+        _load().orc_qblock_attend(_p(qr), qd, _p(kvc), kvd, ps, W, H, Dk, Dv, *map(_p, meta), len(meta[1]) - 1,
+                                  _p(toks), len(toks), _p(un), _p(mem), _p(cnt), int(QB), un.shape[1],
+                                  float(sm_scale), _p(o), _p(lse))
+    return o, lse
 
 
 def dense_mla(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, sm_scale, Dv, tokens=None,
               sliding_window=None, soft_cap=None):
-    """Dense causal absorbed-MLA (the route the backend falls back to): every
-    visible position ``j < min(kv_len, pos+1)``, one position at a time, with
-    a two-pass max/sum softmax. Written independently of ``sparse_mla`` so the
-    property "top-k with k >= kv_len equals dense attention" pins both.
-
-    The backend's dense route (dsa_sparse_backend.py, ``_run_dense``) also
-    passes the layer's ``sliding_window`` and ``logit_cap`` to the dense
-    kernel, whose module the pages do not show; the plain readings taken:
-    a window W keeps the W most recent positions ``pos - W < j <= pos``, and a
-    cap c maps each scaled logit l to ``c * tanh(l / c)`` before the softmax."""
-    kvc = np.asarray(kv)
-    P, ps, Dk_row = kvc.shape
-    seq = token_seq(cu_q_lens)
-    nvis = visible_len(seq_lens, cu_q_lens)
-    pi = np.asarray(page_indices, dtype=np.int64)
-    if tokens is None:
-        tokens = range(len(seq))
-    out = []
-    for t in tokens:
-        s = int(seq[t])
-        qt = widen(q[t])
-        H = qt.shape[0]
-        Dk = qt.shape[-1]
-        n = int(nvis[t])
-        lo = 0
-        if sliding_window:
-            pos = n - 1  # the last visible position is the query's own
-            lo = max(0, pos - int(sliding_window) + 1)
-        if n - lo <= 0:
-            out.append(np.zeros((H, Dv)))
-            continue
-        base = int(cu_kv_lens[s]) // ps
-        logit = np.empty((n - lo, H))
-        vals = np.empty((n - lo, Dv))
-        for j in range(lo, n):
-            row = widen(kvc[pi[base + j // ps], j % ps])
-            l = sm_scale * (qt @ row[:Dk])
-            logit[j - lo] = soft_cap * np.tanh(l / soft_cap) if soft_cap else l
-            vals[j - lo] = row[:Dv]
-        mx = logit.max(axis=0)
-        wgt = np.exp(logit - mx)
-        out.append((wgt.T @ vals) / wgt.sum(axis=0)[:, None])
-    return np.stack(out)
+    """Dense causal MLA (optional sliding window and tanh logit cap): fp64 ``o``."""
+    toks = _tokens(tokens, cu_q_lens)
+    meta = _meta(seq_lens, cu_q_lens, cu_kv_lens, page_indices)
+    qr, qd, kvc, kvd, ps, W = _attend_inputs(q, kv, toks)
+    H, Dk = qr.shape[1], qr.shape[2]
+    o = np.empty((len(toks), H, Dv), np.float64)
+    if len(toks):
+        _load().orc_dense_mla(_p(qr), qd, _p(kvc), kvd, ps, W, H, Dk, Dv, *map(_p, meta), len(meta[1]) - 1,
+                              _p(toks), len(toks), float(sm_scale), int(sliding_window or 0), float(soft_cap or 0.0),
+                              _p(o))
+    return o
 
 
-# ---------------------------------------------------------------------------
-# the step before the path: paged write-back of the new tokens' rows
-# ---------------------------------------------------------------------------
-
+# ------------------------------------------ the step before the path, and next rows
 def paged_write_back(cache, rows, seq_lens, cu_q_lens, cu_kv_lens, page_indices):
-    """Copy of ``cache`` [P, ps, W] with every query token's row written at its
-    own slot (dsa_sparse_backend.py, ``_scatter_paged``): token t of request s
-    lands at absolute position ``pos = kv_len - q_len + (t - q_start)``, i.e.
-    row ``pos % ps`` of physical page ``page_indices[cu_kv_lens[s]//ps +
-    pos//ps]``; the first ``rows.shape[1]`` columns are overwritten. The
-    pages' padding rows (sent to a sentinel page) do not occur here: every
-    token belongs to a request."""
-    out = np.array(cache, copy=True)
-    ps = out.shape[1]
-    D = np.asarray(rows).shape[1]
-    cu = np.asarray(cu_q_lens, dtype=np.int64)
-    seq = token_seq(cu)
-    pos = token_pos(seq_lens, cu)
-    for t in range(int(cu[-1])):
-        s = int(seq[t])
-        entry = int(cu_kv_lens[s]) // ps + int(pos[t]) // ps
-        out[int(page_indices[entry]), int(pos[t]) % ps, :D] = rows[t][:D]
+    """Copy of ``cache`` [P, ps, W] with every query token's row written into
+    its own slot (_scatter_paged); the input is not modified."""
+    out = np.array(cache, copy=True, order="C")
+    src = np.ascontiguousarray(np.asarray(rows).astype(out.dtype))
+    P, ps, W = out.shape
+    D = src.shape[1]
+    meta = _meta(seq_lens, cu_q_lens, cu_kv_lens, page_indices)
+    T = int(meta[1][-1])
+    if T:
+        _load().orc_paged_write_back(_p(out), out.itemsize, ps, W, _p(src), D, *map(_p, meta), len(meta[1]) - 1, T)
     return out
 
 
 def topk_pages_of_tokens(topk_row, ps, cap):
-    """Page list of one query's token selections (dsa_sparse_backend.py,
-    ``compute_topk_pages``, whose module the pages import but do not show;
-    the plain reading): the ascending unique pages ``position // ps`` of the
-    selected tokens, the first ``cap`` of them, -1 padded; also the uncapped
-    number of unique pages."""
-    row = np.asarray(topk_row, dtype=np.int64)
-    uniq = np.unique(row[row >= 0] // ps)
-    out = np.full(cap, -1, dtype=np.int64)
-    n = min(cap, len(uniq))
-    out[:n] = uniq[:n]
-    return out, len(uniq)
+    """(ascending unique pages of one query's tokens, first ``cap``, -1
+    padded; the uncapped number of pages)."""
+    row = _i64(topk_row).reshape(-1)
+    out = np.empty(cap, np.int64)
+    n = _load().orc_topk_pages_of_tokens(_p(row), len(row), int(ps), int(cap), _p(out))
+    return out, int(n)
 
 
 def approx_topk_of_row(scores, k, over):
-    """Approximate top-k of one score row (the pages' fast path uses
-    ``approx_max_k`` with a recall target; this is the two-stage form the
-    build implements, written out): fold the n scores into
-    ``B = min(n, over*k)`` bins (bin b holds positions b, b+B, ...), keep each
-    bin's largest score (lowest position on ties), take the exact top-k of
-    the B bin maxima (ties to the lower bin) and return their positions in
-    ascending order, -1 padded."""
-    s = np.asarray(scores, dtype=np.float32)
-    n = len(s)
-    out = np.full(k, -1, dtype=np.int64)
-    if n == 0:
-        return out
-    B = min(n, over * k)
-    best_pos = np.empty(B, dtype=np.int64)
-    best_val = np.empty(B, dtype=np.float32)
-    for b in range(B):
-        idx = np.arange(b, n, B)
-        j = idx[int(np.argmax(s[idx]))]  # argmax returns the first (lowest) maximum
-        best_pos[b], best_val[b] = j, s[j]
-    bins = topk_of_row(best_val, k)
-    sel = np.sort(best_pos[bins[bins >= 0]])
-    out[: len(sel)] = sel
+    """Two-stage approximate top-k of one row (strided bins of
+    ``min(n, over*k)``, exact top-k of the bin maxima), ascending, -1 padded."""
+    s = _f32(scores)
+    out = np.empty(k, np.int64)
+    _load().orc_approx_topk_row(_p(s), len(s), int(k), int(over), _p(out))
     return out

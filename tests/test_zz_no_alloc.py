@@ -7,7 +7,10 @@ split-key scratch of the decode attention in a device array built into the
 library. This checks, through the C ABI, that two calls in a row (the second
 one finding the first call's leftovers in that array) give the same output
 as the workspace-based entry point, within the attention tolerance of the
-other parity tests.
+other parity tests, and that both match the CPU oracle. The shape is one
+whose key lists are split across CTAs, so the built-in array is in use
+(asserted through the workspace query, which is non-zero exactly when the
+split path runs).
 
 The file name sorts last on purpose: if it fails, a run that stops at the
 first failure has already run every other test.
@@ -17,7 +20,8 @@ import pytest
 import torch
 
 import dsa_inputs as DI
-from gpu_util import ATTN_MAX_ABS, ATTN_REL_L2, meta_to
+import oracle as O
+from gpu_util import ATTN_MAX_ABS, ATTN_REL_L2, check_attention, meta_to
 
 pytestmark = pytest.mark.gpu
 
@@ -55,8 +59,10 @@ def test_noalloc_matches_workspace_entry_point_twice(dsa):
     # split across several CTAs, so the built-in scratch is in use
     wl = DI.random_small(901, [1, 1, 1, 1], [700, 2000, 300, 4000], H=128, k=256)
     rg = wl.rg
+    assert dsa.dsa_sparse_mla_decode_workspace_size(rg.T, 128) > 0, "this shape must take the split-key path"
     meta = meta_to(rg, dev)
     q, kv = wl.q[0].to(dev), wl.kv[0].to(dev)
+    q_np, kv_np = wl.q[0].float().numpy(), wl.kv[0].float().numpy()
     for call, seed in enumerate((1, 2)):
         sel = torch.from_numpy(_selection(rg, 256, seed)).to(dev)
         st = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -67,4 +73,7 @@ def test_noalloc_matches_workspace_entry_point_twice(dsa):
         assert st.item() == 0, f"call {call}: device status {st.item():#x}"
         ok, rel = _close(got, ref)
         assert ok, f"call {call}: rel-L2 {rel:.3e} against dsa_sparse_mla_decode"
+        o_ref, _ = O.sparse_mla(q_np, kv_np, rg.seq_lens, rg.cu_q_lens, rg.cu_kv_lens, rg.page_indices,
+                                sel.cpu().numpy(), 1, wl.sm_scale, 512)
+        check_attention(got, o_ref, f"call {call}: no-allocation entry point against the oracle")
         np.testing.assert_allclose(got_lse.cpu().numpy(), ref_lse.cpu().numpy(), rtol=1e-5, atol=1e-5)
