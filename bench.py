@@ -1,23 +1,29 @@
 #!/usr/bin/env python
 """Benchmark of the DSA sparse-attention hot path on one node.
 
-Default workload: batched decode (32 requests, kv_len ~ U{4096..8192}, pool of
-8192 pages, token top-k k=2048, 128-head absorbed-MLA attention). One step =
-indexer score + exact token top-k + sparse MLA decode over the whole batch.
+Default workload: the ragged mixed batch (48 decode tokens with kv_len
+~ U{8192..131072} plus 4 chunked-prefill extends of 4096 tokens on prefixes
+0/16384/65536/110592; four layers [full, shared, shared, full] with
+IndexShare; token top-k k=2048 and 32-page top-k; query blocks of 256 over
+the block unions; 128-head absorbed-MLA attention). One step = every layer of
+the workload once: on full layers the indexer score + token top-k + page
+top-k + block union, and the sparse MLA attention on every layer.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--only] [--no-cpu-baseline]
 
-Prints ONE JSON line on rank 0. ``--impl reference`` times the CPU oracle (the
-only reference this path has) on a bounded sample of the same workload.
-Multi-GPU runs (torchrun, one rank per GPU) are independent replicas: the path
-has no exchange step; ranks only meet for the timing barrier and the max.
+Prints ONE JSON line on rank 0. Beside the headline workload the line carries
+per-stage numbers of the batched decode, long-context decode and single
+prefill workloads (``workloads``; skipped with ``--only``).
+``--impl reference`` times the CPU oracle (the only reference this path has)
+on a bounded row sample of the same workload. Multi-GPU runs (torchrun, one
+rank per GPU) are independent replicas: the path has no exchange step; ranks
+only meet for the timing barrier and the max.
 """
 from __future__ import annotations
 
 import argparse
-import ctypes
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -38,19 +44,23 @@ KV_LEN_DESC = {
     "single_prefill": "8192 (one request, prefix 0)",
     "ragged_mixed": "decode U{8192..131072}; extends of 4096 on prefixes 0/16384/65536/110592",
 }
+# workloads whose stages ride along in the headline line
+SIDE_WORKLOADS = ("batched_decode", "long_decode", "single_prefill")
 
 L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
+MLA_DK, MLA_DV, IDX_FLOP_PER_PAIR = 576, 512, 2 * 32 * 128
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="batched_decode")
+    ap.add_argument("--workload", default="ragged_mixed")
+    ap.add_argument("--only", action="store_true", help="time the headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -76,21 +86,15 @@ def replica_throughput(tokens_per_step, steps, world, seconds):
     return tokens_per_step * steps * world / seconds
 
 
-# ----------------------------------------------------------------- helpers
-def blas_threads():
-    """Threads of the BLAS numpy runs the oracle's matmuls on."""
+def cpu_model():
     try:
-        with open("/proc/self/maps") as f:
-            libs = {l.split()[-1] for l in f if "openblas" in l.lower() and l.split()[-1].startswith("/")}
-        for path in libs:
-            lib = ctypes.CDLL(path)
-            for fn in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_",
-                       "openblas_get_num_threads", "scipy_openblas_get_num_threads"):
-                if hasattr(lib, fn):
-                    return int(getattr(lib, fn)())
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
     except Exception:
         pass
-    return os.cpu_count() or 1
+    return "unknown"
 
 
 class ClockSampler:
@@ -146,33 +150,34 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def measured_peaks():
+def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            d = json.load(f)
-        return d["hbm_gbs"], "measured"
+            return json.load(f)
     except Exception:
-        return 6800.0, "fallback"
+        return None
+
+
+def measured_peaks():
+    d = _peaks()
+    return (d["hbm_gbs"], "measured") if d else (6800.0, "fallback")
 
 
 def measured_tensor_peak():
     """Dense bf16 peak: the burst figure, since stages are timed alone."""
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            d = json.load(f)
-        return d["bf16_tflops"], "measured (burst)"
-    except Exception:
-        return 1900.0, "fallback"
+    d = _peaks()
+    return (d["bf16_tflops"], "measured (burst)") if d else (1900.0, "fallback")
 
 
-def committed_traffic(kernel_key):
-    """DRAM bytes per launch from a committed ncu summary, only while the
-    kernel source is unchanged since the counters were taken."""
+def committed_traffic(kernel_key, workload):
+    """DRAM bytes per launch from a committed ncu summary, only for the same
+    workload and while the kernel source is unchanged since the counters were
+    taken."""
     import hashlib
 
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            d = json.load(f)[kernel_key]
+            d = json.load(f)[f"{kernel_key}@{workload}"]
         src = os.path.join(ROOT, d["source"])
         h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         return d["bytes_per_launch"] if h == d["source_sha256_16"] else None
@@ -180,32 +185,50 @@ def committed_traffic(kernel_key):
         return None
 
 
-def stage_roofline(wl, rn, timed):
+# ------------------------------------------------------------ work per row
+def row_work(wl, prefill, page_budget=None):
+    """Per query token: visible keys (the indexer's score pairs) and the keys
+    its attention reads (the selection size, capped by what is visible)."""
+    import numpy as np
+
+    rg = wl.rg
+    nvis = np.clip(np.minimum(rg.seq_lens[rg.token_seq()], rg.token_pos() + 1), 0, None).astype(np.int64)
+    if prefill or page_budget is not None:
+        cap = (page_budget or wl.k_pages) * rg.page_size
+    else:
+        cap = wl.k
+    return nvis, np.minimum(nvis, cap)
+
+
+# ------------------------------------------------------------- GPU stages
+def stage_roofline(wl, rn, timed, extras=True):
     """Time every stage of one layer in isolation (L2 flushed before each)
     and set its algorithmic work against the roofline it is bound by:
     decode indexer 256 B per visible key and decode attention 1152 B per
     selected visible key (HBM); prefill indexer 2*32*128 FLOP per visible
     (query, key) pair and query-block attention 2*H*(576+512) FLOP per
-    (query, selected visible key) pair (tensor, bf16). The paged write-back
-    that precedes the path is timed beside them (not part of the step):
-    2 B read + 2 B written per copied element (HBM)."""
+    (query, selected visible key) pair (tensor, bf16). ``per_step`` is how
+    many times the stage runs in one step. With ``extras`` the calls timed
+    beside the step follow: the paged write-back, the dense fallback and the
+    approximate top-k."""
     import numpy as np
     import torch
 
     rg = wl.rg
     hbm, hbm_kind = measured_peaks()
     tfl, tfl_kind = measured_tensor_peak()
-    nvis = np.clip(np.minimum(rg.seq_lens[rg.token_seq()], rg.token_pos() + 1), 0, None).astype(np.int64)
+    nvis, _ = row_work(wl, rn.prefill, rn.page_budget)
     out = {}
+    n_layers, n_full = len(rn.types), rn.num_full
 
-    def entry(ms, work, bound):
+    def entry(ms, work, bound, per_step=1):
         if bound == "hbm":
             ach = work / (ms * 1e-3) / 1e9
-            return {"ms": ms, "algorithmic_bytes": int(work), "bound": "hbm", "achieved": ach, "unit": "GB/s",
-                    "peak": hbm, "peak_kind": hbm_kind, "frac": ach / hbm}
+            return {"ms": ms, "per_step": per_step, "algorithmic_bytes": int(work), "bound": "hbm",
+                    "achieved": ach, "unit": "GB/s", "peak": hbm, "peak_kind": hbm_kind, "frac": ach / hbm}
         ach = work / (ms * 1e-3) / 1e12
-        return {"ms": ms, "algorithmic_flops": int(work), "bound": "tensor", "achieved": ach, "unit": "TFLOP/s",
-                "peak": tfl, "peak_kind": tfl_kind, "frac": ach / tfl}
+        return {"ms": ms, "per_step": per_step, "algorithmic_flops": int(work), "bound": "tensor",
+                "achieved": ach, "unit": "TFLOP/s", "peak": tfl, "peak_kind": tfl_kind, "frac": ach / tfl}
 
     ps = rg.page_size
     if rn.prefill or rn.page_budget is not None:
@@ -214,14 +237,17 @@ def stage_roofline(wl, rn, timed):
     else:
         keys = int((rn.topk[0] >= 0).sum().item())
     if rn.prefill:
-        out["indexer_page_topk"] = entry(timed(lambda: rn.index(0)), 2 * 32 * 128 * nvis.sum(), "tensor")
-        out["block_union"] = entry(timed(lambda: rn.union(0)), rn.topk_pages[0].numel() * 4, "hbm")
-        out["sparse_mla_prefill_qblock"] = entry(timed(lambda: rn.attend(0)), 2 * wl.H * (576 + 512) * keys,
-                                                 "tensor")
+        out["indexer_page_topk"] = entry(timed(lambda: rn.index(0)), IDX_FLOP_PER_PAIR * nvis.sum(), "tensor",
+                                         n_full)
+        out["block_union"] = entry(timed(lambda: rn.union(0)), rn.topk_pages[0].numel() * 4, "hbm", n_full)
+        out["sparse_mla_prefill_qblock"] = entry(timed(lambda: rn.attend(0)),
+                                                 2 * wl.H * (MLA_DK + MLA_DV) * keys, "tensor", n_layers)
     else:
         name = "indexer_page_topk" if rn.page_budget is not None else "indexer_topk"
-        out[name] = entry(timed(lambda: rn.index(0)), 256 * nvis.sum(), "hbm")
-        out["sparse_mla_decode"] = entry(timed(lambda: rn.attend(0)), 1152 * keys, "hbm")
+        out[name] = entry(timed(lambda: rn.index(0)), 256 * nvis.sum(), "hbm", n_full)
+        out["sparse_mla_decode"] = entry(timed(lambda: rn.attend(0)), 1152 * keys, "hbm", n_layers)
+    if not extras:
+        return out
     # the step before the path: paged write-back of every query token's
     # latent row and indexer key (the rows already there are written back
     # unchanged, so the caches keep their contents): 2 x (576 + 128) x 2 B per
@@ -243,7 +269,7 @@ def stage_roofline(wl, rn, timed):
     # the dense fallback (layers without an indexer) over the same queries:
     # every visible position, 1152 B (decode, HBM) or 2*H*(576+512) FLOP
     # (prefill, tensor) per visible (query, key) pair; timed beside the step
-    if args_workload_allows_dense(wl):
+    if wl.name in ("tiny_decode", "batched_decode", "long_decode", "single_prefill"):
         o_dense = torch.empty_like(rn.o[0])
         ws_dense = torch.empty(max(1, dsa.dsa_sparse_mla_decode_workspace_size(rg.T, wl.H)), dtype=torch.uint8,
                                device=rn.kv[0].device)
@@ -254,7 +280,7 @@ def stage_roofline(wl, rn, timed):
 
         pairs = int(nvis.sum())
         if rn.prefill:
-            out["dense_mla"] = entry(timed(dense, reps=3), 2 * wl.H * (576 + 512) * pairs, "tensor")
+            out["dense_mla"] = entry(timed(dense, reps=3), 2 * wl.H * (MLA_DK + MLA_DV) * pairs, "tensor")
         else:
             out["dense_mla"] = entry(timed(dense), 1152 * pairs, "hbm")
         out["dense_mla"]["in_step"] = False
@@ -280,66 +306,164 @@ def stage_roofline(wl, rn, timed):
     return out
 
 
-def args_workload_allows_dense(wl):
-    """The dense fallback is timed on the single-layer workloads (the mixed
-    four-layer batch would take seconds per call)."""
-    return wl.name in ("tiny_decode", "batched_decode", "long_decode", "single_prefill")
+def dominant_stage(kern):
+    """The in-step stage with the most time per step (time x runs per step)."""
+    return max((k for k in kern if kern[k].get("in_step", True)), key=lambda k: kern[k]["ms"] * kern[k]["per_step"])
 
 
 # ---------------------------------------------------------------- oracle leg
-def host_sample(wl, seqs, layer=0):
-    """Compact CPU copy of the requests ``seqs`` of a workload: their query
-    tokens and only their own pages (renumbered), for the CPU oracle."""
+def sample_tokens(wl, n_rows, seed):
+    """A stratified row sample: a third of the rows from the single-token
+    (decode) requests, the rest spread evenly over the multi-token requests,
+    uniformly at random inside each group (seeded)."""
+    import numpy as np
+
+    rg = wl.rg
+    rng = np.random.default_rng(seed)
+    ql = rg.q_lens
+    dec = np.array([int(rg.cu_q_lens[s]) for s in range(rg.S) if ql[s] == 1], np.int64)
+    multi = [s for s in range(rg.S) if ql[s] > 1]
+    n_dec = n_rows if not multi else (min(len(dec), max(1, n_rows // 3)) if len(dec) else 0)
+    picks = list(rng.choice(dec, size=min(len(dec), n_dec), replace=False)) if len(dec) else []
+    if multi:
+        per = max(1, (n_rows - len(picks)) // len(multi))
+        for s in multi:
+            t0 = int(rg.cu_q_lens[s])
+            picks += list(t0 + rng.choice(int(ql[s]), size=min(int(ql[s]), per), replace=False))
+    return sorted(int(t) for t in picks)
+
+
+def _host_bits(t):
+    """bf16 tensor -> uint16 numpy bit patterns (exact, half the bytes of fp32);
+    fp32 tensors stay fp32."""
+    import torch
+
+    if t.dtype == torch.bfloat16:
+        return t.contiguous().view(torch.int16).cpu().numpy().view("uint16")
+    return t.float().cpu().numpy()
+
+
+def oracle_sample_seconds(wl, tokens, prefill, page_budget=None):
+    """Oracle time of one step (every layer of the workload) over the sampled
+    rows ``tokens``: per full layer the indexer score + token top-k (+ page
+    top-k), per layer the sparse MLA attention over the row's selection (page
+    units on the prefill path: the per-query form, which the oracle pins equal
+    to the query-block form). Host copies of the rows and pages the sample
+    touches are made outside the timed calls. Returns the seconds."""
     import numpy as np
     import torch
 
-    rg = wl.rg
-    ps = rg.page_size
-    pages, pi, cu_kv, toks = [], [], [0], []
-    for s in seqs:
-        npg = -(-int(rg.seq_lens[s]) // ps)
-        b = int(rg.cu_kv_lens[s]) // ps
-        pi.extend(range(len(pages), len(pages) + npg))
-        pages.extend(rg.page_indices[b:b + npg].tolist())
-        cu_kv.append(cu_kv[-1] + npg * ps)
-        toks.extend(range(int(rg.cu_q_lens[s]), int(rg.cu_q_lens[s + 1])))
-    dev = wl.kcache[0].device
-    pidx = torch.tensor(pages, dtype=torch.long, device=dev)
-    tidx = torch.tensor(toks, dtype=torch.long, device=dev)
-    f = lambda t: t.float().cpu().numpy()
-    q_lens = np.diff(rg.cu_q_lens)[list(seqs)]
-    return dict(
-        q_idx=f(wl.q_idx.to(dev)[tidx]), w=f(wl.w.to(dev)[tidx]), kcache=f(wl.kcache[0][pidx]),
-        q=f(wl.q[layer].to(dev)[tidx]), kv=f(wl.kv[layer][pidx]),
-        seq_lens=rg.seq_lens[list(seqs)].copy(),
-        cu_q_lens=np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32),
-        cu_kv_lens=np.asarray(cu_kv, np.int32), page_indices=np.asarray(pi, np.int32), ntok=len(toks))
-
-
-def oracle_decode_step(smp, k, sm_scale):
     import oracle as O
 
-    meta = dict(seq_lens=smp["seq_lens"], cu_q_lens=smp["cu_q_lens"], cu_kv_lens=smp["cu_kv_lens"],
-                page_indices=smp["page_indices"])
-    topk, _ = O.indexer_topk(smp["q_idx"], smp["w"], smp["kcache"], k=k, **meta)
-    o, _ = O.sparse_mla(smp["q"], smp["kv"], sel=topk, unit=1, sm_scale=sm_scale, Dv=512, **meta)
-    return o
-
-
-def time_oracle(wl, min_seconds=10.0, max_seconds=30.0):
-    """Oracle throughput on a bounded sample: requests are taken one at a
-    time, in order (wrapping around), until at least ``min_seconds`` of CPU
-    work has been timed."""
-    total, toks, nreq = 0.0, 0, 0
-    S = wl.rg.S
-    while total < min_seconds and total < max_seconds:
-        smp = host_sample(wl, [nreq % S])
+    rg = wl.rg
+    ps = rg.page_size
+    tseq = rg.token_seq()
+    seqs = sorted({int(tseq[t]) for t in tokens})
+    # compact batch of the sampled requests: all their query tokens (positions
+    # depend on q_len) and their page-table entries, renumbered
+    q_lens = rg.q_lens[seqs]
+    cu_q = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int64)
+    npg = -(-rg.seq_lens[seqs].astype(np.int64) // ps)
+    cu_kv = np.concatenate([[0], np.cumsum(npg * ps)]).astype(np.int64)
+    ent = np.concatenate([int(rg.cu_kv_lens[s]) // ps + np.arange(n) for s, n in zip(seqs, npg)])
+    phys = rg.page_indices[ent].astype(np.int64)
+    pos_of = {s: i for i, s in enumerate(seqs)}
+    ctok = [int(cu_q[pos_of[int(tseq[t])]] + t - int(rg.cu_q_lens[int(tseq[t])])) for t in tokens]
+    meta = dict(seq_lens=rg.seq_lens[seqs].astype(np.int64), cu_q_lens=cu_q, cu_kv_lens=cu_kv)
+    dev = wl.kcache[0].device
+    tidx = torch.tensor(tokens, dtype=torch.long, device=wl.q_idx.device)
+    q_idx = dict(zip(ctok, _host_bits(wl.q_idx.index_select(0, tidx))))
+    w = dict(zip(ctok, _host_bits(wl.w.index_select(0, tidx.to(wl.w.device)))))
+    pidx = torch.from_numpy(phys).to(dev)
+    types = list(wl.indexer_types) if wl.indexer_types else [0]
+    full_slot, src_slot, nfull = O.build_index_share_map(["full" if x == 0 else "shared" for x in types], 0,
+                                                         len(types))
+    kcaches = [_host_bits(wl.kcache[i].index_select(0, pidx)) for i in range(nfull)]
+    pi_idx = np.arange(len(phys), dtype=np.int64)  # the compacted indexer pools are in page-table order
+    seconds = 0.0
+    sels = {}
+    use_pages = prefill or page_budget is not None
+    for slot in range(nfull):
         t0 = time.perf_counter()
-        oracle_decode_step(smp, wl.k, wl.sm_scale)
-        total += time.perf_counter() - t0
-        toks += smp["ntok"]
-        nreq += 1
-    return toks / total, total, toks, nreq
+        if use_pages:
+            sel, rows = O.indexer_page_topk(q_idx, w, kcaches[slot], page_indices=pi_idx,
+                                            k_pages=page_budget or wl.k_pages, tokens=ctok, **meta)
+            if prefill:  # the prefill step also keeps the token top-k
+                O.topk_rows_of(rows, wl.k)
+        else:
+            sel, rows = O.indexer_topk(q_idx, w, kcaches[slot], page_indices=pi_idx, k=wl.k, tokens=ctok,
+                                       **meta)
+        seconds += time.perf_counter() - t0
+        sels[slot] = sel
+    for layer in range(len(types)):
+        sel = sels[src_slot[layer]]
+        # attention pool: the physical pages the selections name, plus a zero page
+        need = set()
+        for i, t in enumerate(ctok):
+            s = pos_of[int(tseq[tokens[i]])]
+            row = sel[i][sel[i] >= 0].astype(np.int64)
+            pages = row if use_pages else np.unique(row // ps)
+            need.update((int(cu_kv[s]) // ps + pages).tolist())
+        need = np.array(sorted(need), np.int64)
+        apool = _host_bits(wl.kv[layer].index_select(0, torch.from_numpy(phys[need]).to(dev)))
+        apool = np.concatenate([np.zeros((1,) + apool.shape[1:], apool.dtype), apool])
+        api = np.zeros(len(phys), np.int64)
+        api[need] = np.arange(1, len(need) + 1)
+        qrows = dict(zip(ctok, _host_bits(wl.q[layer].index_select(0, tidx.to(wl.q[layer].device)))))
+        selrows = dict(zip(ctok, sel))
+        t0 = time.perf_counter()
+        O.sparse_mla(qrows, apool, page_indices=api, sel=selrows, unit=ps if use_pages else 1,
+                     sm_scale=wl.sm_scale, Dv=MLA_DV, tokens=ctok, **meta)
+        seconds += time.perf_counter() - t0
+    return seconds
+
+
+def oracle_estimate(wl, tokens, prefill, page_budget=None):
+    """The oracle's time for one full step of the workload, extrapolated from
+    the sampled rows by counted work: the oracle's loops cost in proportion to
+    its score pairs (2*32*128 FLOP each, per full layer) and attended keys
+    (2*H*(576+512) FLOP each, per layer; counted as the selection size capped
+    by the visible prefix), so the full step is estimated at the sample's
+    seconds x full work / sample work."""
+    import numpy as np
+
+    secs = oracle_sample_seconds(wl, tokens, prefill, page_budget)
+    types = list(wl.indexer_types) if wl.indexer_types else [0]
+    nfull, nl = sum(1 for x in types if x == 0), len(types)
+    nvis, att = row_work(wl, prefill, page_budget)
+    flop_att = 2 * wl.H * (MLA_DK + MLA_DV)
+
+    def work(idx):
+        return nfull * IDX_FLOP_PER_PAIR * float(nvis[idx].sum()) + nl * flop_att * float(att[idx].sum())
+
+    w_full = work(slice(None))
+    w_smp = work(np.asarray(tokens, np.int64))
+    return secs * w_full / max(w_smp, 1.0), secs, len(tokens)
+
+
+def _workload_device():
+    import torch
+
+    return torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else torch.device("cpu")
+
+
+def cpu_baseline_line(wl, prefill, page_budget, name, target_s=15.0):
+    """The oracle on the host cores on a bounded row sample of the workload,
+    extrapolated to one full step by counted work, as tokens/s."""
+    import oracle as O
+
+    n = 64 if prefill else 48
+    toks = sample_tokens(wl, n, seed=1)
+    est, secs, nrow = oracle_estimate(wl, toks, prefill, page_budget)
+    if secs < target_s / 3 and nrow < wl.rg.T:  # too small to time well: one larger sample
+        scale = min(8.0, target_s / max(secs, 1e-3))
+        toks = sample_tokens(wl, int(n * scale), seed=2)
+        est, secs, nrow = oracle_estimate(wl, toks, prefill, page_budget)
+    return {"value": wl.rg.T / est, "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
+            "cpu": cpu_model(), "oracle_seconds": secs, "extrapolated_step_s": est,
+            "sample": f"{nrow} of {wl.rg.T} query rows of {name} (stratified: decode rows and rows spread "
+                      f"over every extend), every layer of the step on those rows; the step's time is "
+                      f"extrapolated from the sample by counted work (score pairs and attended keys)"}
 
 
 # --------------------------------------------------------------- reference
@@ -348,29 +472,33 @@ def run_reference(args):
     if rank != 0:
         return 0
     import dsa_inputs as DI
+    import oracle as O
 
-    wl = DI.WORKLOADS[args.workload]()
-    S = wl.rg.S
-    cores = blas_threads()
-    times, toks = [], 0
+    dev = _workload_device()
+    wl = DI.WORKLOADS[args.workload](device=dev)
+    rg = wl.rg
+    prefill = bool((rg.q_lens > 1).any())
+    rows_per_step = 16
+    ests, secs, nrows = [], 0.0, 0
     for i in range(args.warmup + args.steps):
-        s = i % S
-        smp = host_sample(wl, [s])
-        t0 = time.perf_counter()
-        oracle_decode_step(smp, wl.k, wl.sm_scale)
-        dt = time.perf_counter() - t0
+        toks = sample_tokens(wl, rows_per_step, seed=100 + i)
+        est, s, n = oracle_estimate(wl, toks, prefill)
         if i >= args.warmup:
-            times.append(dt)
-            toks += smp["ntok"]
-    total = sum(times)
-    value = toks / total
+            ests.append(est)
+            secs += s
+            nrows += n
+    total = sum(ests)
+    value = rg.T * args.steps / total
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-        "config": {"workload": args.workload, "sample": "one request (its decode token) per step"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{args.steps} requests of the {args.workload} workload, one per step"},
+        "config": {"workload": args.workload, "tokens_per_step": rg.T, "layers": len(wl.indexer_types or [0]),
+                   "sample": f"{rows_per_step} query rows per step (stratified), extrapolated by counted work"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
+                         "cpu": cpu_model(), "oracle_seconds": secs,
+                         "sample": f"{nrows} query rows of {args.workload} over {args.steps} steps; each step's "
+                                   f"time extrapolated from its rows by counted work"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -378,8 +506,90 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------- ours
+def make_timer(flush):
+    import torch
+
+    def timed(fn, reps=10):
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    return timed
+
+
+def capture_step(rn, dev, warmup):
+    """CUDA graph of one step (the launch overhead of the small kernels
+    removed), or None if capture fails."""
+    import torch
+
+    try:
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(s):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                rn.step()
+        torch.cuda.current_stream(dev).wait_stream(s)
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        return g
+    except Exception:  # pragma: no cover - reported in the JSON line
+        torch.cuda.synchronize()
+        return None
+
+
+def time_steps(run, flush, steps):
+    import torch
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record()
+        run()
+        ends[i].record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+
+
+def side_workload(name, dev, flush, args):
+    """Step time and per-stage rooflines of another workload (one layer per
+    step), for the headline line's ``workloads`` object."""
+    import torch
+
+    import dsa_inputs as DI
+    from deepseek_sparse_attention_score_gb300.layer import LayerRunner
+
+    wl = DI.WORKLOADS[name](device=dev)
+    rn = LayerRunner(wl, dev)
+    for _ in range(max(1, args.warmup)):
+        rn.step()
+    torch.cuda.synchronize()
+    assert rn.status.item() == 0, f"{name}: device status {rn.status.item():#x}"
+    g = capture_step(rn, dev, args.warmup)
+    ms = time_steps(g.replay if g is not None else rn.step, flush, args.steps)
+    timed = make_timer(flush)
+    kern = stage_roofline(wl, rn, timed)
+    step_ms = sum(ms) / len(ms)
+    res = {"tokens_per_s": rn.T / (step_ms * 1e-3), "ms_per_step": step_ms, "tokens_per_step": rn.T,
+           "kv_len": KV_LEN_DESC.get(name), "cuda_graph": g is not None, "kernels": kern}
+    dom = dominant_stage(kern)
+    res["dominant"] = {"kernel": dom, "frac": kern[dom]["frac"], "bound": kern[dom]["bound"],
+                       "traffic": committed_traffic(dom, name)}
+    del rn, wl, g
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
-    import numpy as np
     import torch
 
     rank, world, local = dist_env()
@@ -415,75 +625,41 @@ def run_ours(args):
     launches_per_step = dsa.dsa_launch_count() - c0
     assert rn.status.item() == 0, f"device status {rn.status.item():#x}"
 
-    # CUDA graph of one step (launch overhead of the ~6 small kernels removed)
-    graph = None
-    try:
-        s = torch.cuda.Stream(dev)
-        s.wait_stream(torch.cuda.current_stream(dev))
-        with torch.cuda.stream(s):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=s):
-                rn.step()
-        torch.cuda.current_stream(dev).wait_stream(s)
-        for _ in range(args.warmup):
-            g.replay()
-        torch.cuda.synchronize()
-        graph = g
-    except Exception as e:  # pragma: no cover - reported in the JSON line
-        graph_err = repr(e)[:200]
+    graph = capture_step(rn, dev, args.warmup)
     run = graph.replay if graph is not None else rn.step
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     with ClockSampler(torch.cuda.current_device()) as clk:
         # keep the GPU busy with back-to-back steps for ~1.5 s around the timed
         # steps so the 200 ms clock samples land under the same load
         t_end = time.perf_counter() + 1.0
         while time.perf_counter() < t_end:
-            for _ in range(20):
+            for _ in range(4):
                 flush.zero_()
                 run()
             torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
         w0 = time.perf_counter()
-        for i in range(args.steps):
-            flush.zero_()
-            starts[i].record()
-            run()
-            ends[i].record()
-        torch.cuda.synchronize()
+        step_ms = time_steps(run, flush, args.steps)
         wall = time.perf_counter() - w0
         barrier()
         t_end = time.perf_counter() + 0.5
         while time.perf_counter() < t_end:
-            for _ in range(20):
+            for _ in range(4):
                 flush.zero_()
                 run()
             torch.cuda.synchronize()
-    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     total_s = max_over_ranks(sum(step_ms) / 1e3, world)
     value = replica_throughput(T, args.steps, world, total_s)
     clocks = clk.summary()
 
     # per-ABI-call times (eager, L2 flushed before each) for the roofline
-    def timed(fn, reps=10):
-        ts = []
-        for _ in range(reps):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        return statistics.median(ts)
-
+    timed = make_timer(flush)
     kern = stage_roofline(wl, rn, timed)
-    dom = max((k for k in kern if kern[k].get("in_step", True)), key=lambda k: kern[k]["ms"])
+    dom = dominant_stage(kern)
     d = kern[dom]
     roof = {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"], "unit": d["unit"],
-            "frac": d["frac"], "peak_kind": d["peak_kind"], "traffic": committed_traffic(dom)}
+            "frac": d["frac"], "peak_kind": d["peak_kind"], "traffic": committed_traffic(dom, args.workload)}
 
     # end to end through the public API with host buffers
     pin = lambda t: t.detach().to("cpu").pin_memory()
@@ -518,42 +694,39 @@ def run_ours(args):
     for _ in range(args.warmup):
         e2e_step()
     torch.cuda.synchronize()
-    e_ms = []
-    for _ in range(args.steps):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        e2e_step()
-        b.record()
-        torch.cuda.synchronize()
-        e_ms.append(a.elapsed_time(b))
-    e2e_s = max_over_ranks(sum(e_ms) / 1e3, world)
+    e_ms = make_timer(flush)
+    e_list = [e_ms(e2e_step, reps=1) for _ in range(args.steps)]
+    e2e_s = max_over_ranks(sum(e_list) / 1e3, world)
     e2e = {"value": replica_throughput(T, args.steps, world, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * e2e_s / args.steps, "cuda_graph": e2e_graph}
 
     cpu = None
-    decode_workload = not rn.prefill and rn.page_budget is None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and decode_workload:
-        v, dt, ntok, nreq = time_oracle(wl)
-        cpu = {"value": v, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-               "sample": f"{nreq} requests of the {args.workload} workload taken in order ({ntok} decode "
-                         f"tokens: indexer + top-k + sparse MLA), {dt:.1f} s of CPU time"}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_line(wl, rn.prefill, rn.page_budget, args.workload)
+
+    config = {"workload": args.workload, "requests": wl.rg.S, "tokens_per_step": T, "layers": len(rn.types),
+              "kv_len": KV_LEN_DESC.get(args.workload, "per request, from the workload"),
+              "k": wl.k, "k_pages": wl.k_pages, "mla_heads": wl.H, "page_size": wl.rg.page_size,
+              "l2": "flushed (512 MB write) before every timed step", "cuda_graph": graph is not None,
+              "parallelism": "replicas" if world > 1 else "single"}
+    # free the headline workload before the side workloads are built
+    del rn, wl, graph, h_q, h_o, h_q_idx, h_w, h_meta, h_topk
+    torch.cuda.empty_cache()
+    sides = {}
+    if not args.only and rank == 0 and world == 1:
+        for name in SIDE_WORKLOADS:
+            if name != args.workload:
+                sides[name] = side_workload(name, dev, flush, args)
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": args.workload, "requests": wl.rg.S, "tokens_per_step": T,
-                       "layers": len(rn.types),
-                       "kv_len": KV_LEN_DESC.get(args.workload, "per request, from the workload"),
-                       "k": wl.k, "mla_heads": wl.H, "page_size": wl.rg.page_size,
-                       "l2": "flushed (512 MB write) before every timed step", "cuda_graph": graph is not None,
-                       "parallelism": "replicas" if world > 1 else "single"},
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
             "roofline": roof, "kernels": kern, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps, "launches_per_step": launches_per_step,
             "clocks": clocks, "clock_window": "1.5 s of back-to-back steps enclosing the timed steps",
-            "wall_s_timed_region": wall,
+            "wall_s_timed_region": wall, "workloads": sides,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -261,6 +261,20 @@ def page_topk_of_row(scores, ps, k_pages) -> np.ndarray:
     return out[0].astype(np.int32)
 
 
+def topk_rows_of(rows, k) -> np.ndarray:
+    """Exact top-k [n, k] int32 of a list of score rows (as topk_of_row)."""
+    n = len(rows)
+    lens = _i64([len(r) for r in rows])
+    ld = max(1, int(lens.max()) if n else 1)
+    mat = np.zeros((n, ld), np.float32)
+    for i, r in enumerate(rows):
+        mat[i, : len(r)] = r
+    out = np.empty((n, k), np.int64)
+    if n:
+        _load().orc_topk_rows(_p(mat), ld, _p(lens), n, k, _p(out))
+    return out.astype(np.int32)
+
+
 def indexer_topk(q, w, kcache, seq_lens, cu_q_lens, cu_kv_lens, page_indices, k, tokens=None):
     """(token top-k [n, k] int32, score rows) of the given tokens."""
     out, lens, toks, _ = _score_matrix(q, w, kcache, seq_lens, cu_q_lens, cu_kv_lens, page_indices, tokens)
