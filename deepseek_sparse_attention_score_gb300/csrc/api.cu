@@ -211,7 +211,8 @@ size_t dsa_indexer_workspace_size(int T, int S, int max_kv, int ps) {
 // their positions [T, B], bin counts [T] and the selected bins [T, k]
 static size_t approx_bins(int k, int over, int max_kv) {
   const long long kb = (long long)k * over;
-  return (size_t)(kb < max_kv ? kb : max_kv);
+  const size_t b = (size_t)(kb < max_kv ? kb : max_kv);
+  return (b + 3) & ~(size_t)3;  // the row stride of the bin maxima: a multiple of four
 }
 static size_t approx_extra(int T, int k, int over, int max_kv) {
   const size_t B = approx_bins(k, over, max_kv);

@@ -81,16 +81,17 @@ int run_topk_approx(cudaStream_t stream, const float* scores, long long ld, cons
   if (T == 0) return DSA_OK;
   const long long kb = (long long)k * over;
   const int bmax = (int)(kb < max_kv ? kb : max_kv);
+  const int ldb = (bmax + 3) & ~3;  // bin rows start 16-byte aligned (the top-k reads them as float4)
   dim3 g1(T, (bmax + kBinThreads - 1) / kBinThreads);
   approx_bins_kernel<<<g1, kBinThreads, 0, stream>>>(scores, ld, nvis, (int)(kb < (1LL << 30) ? kb : (1LL << 30)),
-                                                     vals, pos, nb, bmax);
+                                                     vals, pos, nb, ldb);
   DSA_CHECK_LAUNCH();
-  int rc = run_topk(stream, vals, bmax, nb, T, 1, k, cand, nullptr, bmax);
+  int rc = run_topk(stream, vals, ldb, nb, T, 1, k, cand, nullptr, bmax);
   if (rc) return rc;
   int n_pow2 = 1;
   while (n_pow2 < k) n_pow2 <<= 1;
   set_smem_attr_once(reinterpret_cast<const void*>(approx_finish_kernel), approx_max_k() * 4);
-  approx_finish_kernel<<<T, kFinThreads, (size_t)n_pow2 * 4, stream>>>(cand, k, pos, bmax, out, n_pow2);
+  approx_finish_kernel<<<T, kFinThreads, (size_t)n_pow2 * 4, stream>>>(cand, k, pos, ldb, out, n_pow2);
   DSA_CHECK_LAUNCH();
   return DSA_OK;
 }

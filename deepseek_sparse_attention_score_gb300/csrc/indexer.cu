@@ -162,8 +162,9 @@ __global__ void __launch_bounds__(1024) indexer_plan_kernel(IndexerMeta m, Index
 // ------------------------------------------------------------------ scorer
 template <int NQ>
 struct IdxCfg {
-  static constexpr int N = NQ * 32;                 // UMMA N: (query, head) columns
-  static constexpr int EPI_WARPS = NQ == 1 ? 4 : 8;  // epilogue warps
+  static constexpr int N = NQ * 32;                  // UMMA N: (query, head) columns
+  static constexpr int EPI_WARPS = NQ == 1 ? 4 : 16;  // epilogue warps: 1 or 4 per TMEM lane quadrant
+  static constexpr int QPW = NQ / (EPI_WARPS / 4);    // queries each epilogue warp scores per tile
   static constexpr int THREADS = 64 + EPI_WARPS * 32;
   static constexpr int STAGES = NQ == 1 ? 6 : 3;
   static constexpr int Q_BYTES = N * 256;            // N rows x 128 dims bf16
@@ -173,17 +174,23 @@ struct IdxCfg {
   static constexpr int OFF_STAGE = 2 * Q_BYTES;
   static constexpr int OFF_W = OFF_STAGE + STAGES * STAGE_BYTES;
   static constexpr int OFF_PMAX = OFF_W + 2 * N * 4;
-  static constexpr int OFF_BAR = OFF_PMAX + 2 * NQ * 4 * 4;
+  // page max-pool slots {ordered key, arrivals} per (tile mod 4, query, page of the tile)
+  static constexpr int PM_SLOTS = 4 * NQ * 2;
+  static constexpr int OFF_BAR = OFF_PMAX + PM_SLOTS * 8;
   static constexpr int NBAR = 2 * STAGES + 9;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
   static constexpr uint32_t IDESC = make_idesc_bf16(128, N, false, false);
 };
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
+// Order-preserving map fp32 -> uint32 (larger float -> larger key; 0 is
+// below every mapped value), and its inverse.
+__device__ __forceinline__ uint32_t ordered_key_f32(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float ordered_key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
 template <int NQ>
@@ -202,7 +209,8 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::THREADS, 1)
   uint8_t* q_s = smem + C::OFF_Q;
   uint8_t* st_s = smem + C::OFF_STAGE;
   float* w_s = reinterpret_cast<float*>(smem + C::OFF_W);
-  float* pmax_s = reinterpret_cast<float*>(smem + C::OFF_PMAX);
+  uint32_t* pm_key = reinterpret_cast<uint32_t*>(smem + C::OFF_PMAX);
+  uint32_t* pm_cnt = pm_key + C::PM_SLOTS;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::STAGES;
@@ -229,6 +237,7 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::THREADS, 1)
     }
     mbar_init(fin, 1);
     *abort_flag = 0;
+    for (int i = 0; i < 2 * C::PM_SLOTS; ++i) pm_key[i] = 0u;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -357,10 +366,15 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::THREADS, 1)
     }
   } else {
     // ---------------------------------------------------------- epilogue
+    // Warp ew reads TMEM lane quadrant ew % 4 (keys quad*32 .. +31 of the
+    // tile) and scores queries [QPW*qset, QPW*qset + QPW) of the tile: the
+    // QPW 32-column slices are loaded together and waited for once, then each
+    // score is a ReLU-weighted head sum with four independent accumulators
+    // (head weights read four at a time from shared memory).
     const int ew = warp - 2;
-    const int quad = warp & 3;        // TMEM lane quadrant this warp may access
-    const int qset = ew >> 2;         // NQ = 8: queries [4*qset, 4*qset + 4)
-    constexpr int QPW = NQ == 1 ? 1 : 4;
+    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    const int qset = ew >> 2;
+    constexpr int QPW = C::QPW;
     const int ps = m.ps;
     int dt = 0, it = 0;
     bool ok = true;
@@ -371,7 +385,7 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::THREADS, 1)
       int nv[QPW];
 #pragma unroll
       for (int j = 0; j < QPW; ++j) {
-        const int q = qset * 4 + j;
+        const int q = qset * QPW + j;
         nv[j] = q < ntok ? pl.nvis[t0 + q] : 0;
       }
       if (!(ok = mbar_wait(qfull + qb, (it >> 1) & 1, abort_flag))) break;
@@ -381,43 +395,61 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::THREADS, 1)
         if (!(ok = mbar_wait(dfull + db, (dt >> 1) & 1, abort_flag))) break;
         tc_fence_after();
         const int key = tile * 128 + quad * 32 + lane;
+        uint32_t r[QPW][32];
+        const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + db * C::N + qset * QPW * 32;
+#pragma unroll
+        for (int j = 0; j < QPW; ++j) tmem_ld32(taddr + j * 32, r[j]);
+        tmem_ld_wait_regs(r[0]);
+#pragma unroll
+        for (int j = 1; j < QPW; ++j) reg_fence(r[j]);
+        // the D buffer is free as soon as the values are in registers
+        tc_fence_before();
+        mbar_arrive(dempty + db);
 #pragma unroll
         for (int j = 0; j < QPW; ++j) {
-          const int q = qset * 4 + j;
+          const int q = qset * QPW + j;
           if (q >= ntok) break;  // warp-uniform
-          uint32_t r[32];
-          tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + db * C::N + q * 32, r);
-          tmem_ld_wait();
-          float sc = 0.f;
+          const float4* w4 = reinterpret_cast<const float4*>(wq + q * 32);
+          uint64_t acc[2] = {0ull, 0ull};  // four partial sums in two packed pairs
 #pragma unroll
-          for (int h = 0; h < 32; ++h) sc = fmaf(fmaxf(__uint_as_float(r[h]), 0.f), wq[q * 32 + h], sc);
+          for (int h4 = 0; h4 < 8; ++h4) {
+            const float4 wv = w4[h4];
+            const float a0 = fmaxf(__uint_as_float(r[j][4 * h4 + 0]), 0.f);
+            const float a1 = fmaxf(__uint_as_float(r[j][4 * h4 + 1]), 0.f);
+            const float a2 = fmaxf(__uint_as_float(r[j][4 * h4 + 2]), 0.f);
+            const float a3 = fmaxf(__uint_as_float(r[j][4 * h4 + 3]), 0.f);
+            acc[0] = ffma2(f32x2_pack(a0, a1), f32x2_pack(wv.x, wv.y), acc[0]);
+            acc[1] = ffma2(f32x2_pack(a2, a3), f32x2_pack(wv.z, wv.w), acc[1]);
+          }
+          float s0, s1, s2, s3;
+          f32x2_unpack(acc[0], s0, s1);
+          f32x2_unpack(acc[1], s2, s3);
+          const float sc = (s0 + s1) + (s2 + s3);
           const bool valid = key >= kb && key < ke && key < nv[j];
           if (out.tok_scores && valid) out.tok_scores[(size_t)(t0 + q) * out.ld_tok + key] = sc;
           if (out.page_scores) {
-            const float pm = warp_max(valid ? sc : -INFINITY);
+            const float pm = warp_max_f32(valid ? sc : -INFINITY);
+            const int qkey0 = tile * 128 + quad * 32;  // first key of this quadrant
             if (ps == 32) {
-              if (lane == 0 && tile * 128 + quad * 32 < nv[j] && tile * 128 + quad * 32 >= kb)
-                out.page_scores[(size_t)(t0 + q) * out.ld_pg + (tile * 128 + quad * 32) / 32] = pm;
+              if (lane == 0 && qkey0 < nv[j] && qkey0 >= kb)
+                out.page_scores[(size_t)(t0 + q) * out.ld_pg + qkey0 / 32] = pm;
             } else if (lane == 0) {
-              pmax_s[(db * NQ + q) * 4 + quad] = pm;
-            }
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(dempty + db);
-        if (out.page_scores && ps > 32) {
-          named_bar_sync(1, EPI_THREADS);
-          // one lane per (query, page of this tile)
-          const int ppt = 128 / ps, qpp = ps / 32;
-          if (ew == 0 && lane < NQ * ppt) {
-            const int q = lane / ppt, pg = lane % ppt;
-            const int key0 = tile * 128 + pg * ps;
-            if (q < ntok) {
-              const int nvq = pl.nvis[t0 + q];
-              if (key0 < nvq && key0 < ke && key0 >= kb) {
-                float pm = -INFINITY;
-                for (int u = 0; u < qpp; ++u) pm = fmaxf(pm, pmax_s[(db * NQ + q) * 4 + pg * qpp + u]);
-                out.page_scores[(size_t)(t0 + q) * out.ld_pg + key0 / ps] = pm;
+              // a page spans ps / 32 quadrants (warps): each folds its maximum
+              // into the page's slot; the last to arrive writes the page score
+              // and clears the slot. A warp runs at most two tiles ahead of
+              // the slowest one (the D buffers hold it), so slots rotate over
+              // four tiles.
+              const int qpp = ps / 32, pg = quad / qpp;
+              const int slot = (((dt & 3) * NQ + q) * 2) + pg;
+              atomicMax(pm_key + slot, ordered_key_f32(pm));
+              __threadfence_block();
+              if (atomicAdd(pm_cnt + slot, 1u) == (uint32_t)(qpp - 1)) {
+                __threadfence_block();
+                const uint32_t mk = atomicExch(pm_key + slot, 0u);
+                atomicExch(pm_cnt + slot, 0u);
+                const int key0 = tile * 128 + pg * ps;
+                if (key0 < nv[j] && key0 < ke && key0 >= kb)
+                  out.page_scores[(size_t)(t0 + q) * out.ld_pg + key0 / ps] = ordered_key_value(mk);
               }
             }
           }

@@ -105,10 +105,12 @@ __device__ __forceinline__ void pick_digit(uint32_t* hist, int shift, uint32_t& 
 // Ordered emission: every index with key > kstar, plus the lowest-index
 // need_eq copies of kstar, in ascending index order. Warp w owns a contiguous
 // segment; two block scans give each warp its output offset.
+// With s_idx, entry i of the staged keys stands for row position s_idx[i]
+// (a compacted candidate list kept in ascending position order).
 template <bool kStaged>
 __device__ void emit_ordered(const float* __restrict__ g, const uint32_t* __restrict__ s_row, int n,
                              uint32_t kstar, int need_eq, int32_t* __restrict__ out_idx, float* __restrict__ out_val,
-                             int* s_tmp) {
+                             int* s_tmp, const int* __restrict__ s_idx = nullptr) {
   const int w = warp_id(), lane = lane_id();
   auto key_at = [&](int i) -> uint32_t { return kStaged ? s_row[i] : ordered_key(__ldg(g + i)); };
   const int seg = ((n + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
@@ -137,8 +139,9 @@ __device__ void emit_ordered(const float* __restrict__ g, const uint32_t* __rest
     const uint32_t selb = __ballot_sync(0xffffffffu, sel);
     if (sel) {
       const int pos = sel_run + __popc(selb & lt);
-      out_idx[pos] = i;
-      if (out_val) out_val[pos] = __ldg(g + i);
+      const int j = s_idx ? s_idx[i] : i;
+      out_idx[pos] = j;
+      if (out_val) out_val[pos] = __ldg(g + j);
     }
     eq_run += __popc(eqb);
     sel_run += __popc(selb);
@@ -280,6 +283,181 @@ __device__ void select_row_global(const float* __restrict__ g, int n, int k, int
   }
 }
 
+// Row longer than shared memory, in two reads of the row instead of one per
+// radix digit:
+//  A. every warp histograms the top kWideBits bits of the keys of its own
+//     contiguous segment of the row (a 2048-bin histogram per warp); the sums
+//     give the bin b* that holds the rank-k key;
+//  B. every warp copies, in position order, the keys of its segment whose top
+//     bits are >= b* (exactly the candidates: every winner, plus the rest of
+//     bin b*) into a shared-memory list; the per-warp histograms give each
+//     warp its offset, so the list is in ascending position order;
+//  C. the exact radix select and the ordered emission run on that list.
+// Returns false (before writing anything) when the candidates would not fit;
+// the caller then takes the multi-pass path.
+constexpr int kWideBits = 11;
+constexpr int kWideBins = 1 << kWideBits;
+constexpr int kWideShift = 32 - kWideBits;
+constexpr int kCandCap = kTopkSmemCap / 2;  // candidates: keys + positions in the staging area
+static_assert(kTopkWarps * kWideBins <= kTopkSmemCap, "per-warp wide histograms fit the staging area");
+static_assert(kTopkThreads * 4 == kWideBins, "four wide bins per thread");
+
+__device__ bool select_row_two_pass(const float* __restrict__ g, int n, int k, int32_t* __restrict__ out_idx,
+                                    float* __restrict__ out_val, uint32_t* hist, uint32_t* area, int* s_tmp) {
+  const int tid = threadIdx.x, w = warp_id(), lane = lane_id();
+  __shared__ int s_sel[2];
+  __shared__ int s_woff[kTopkWarps + 1];
+  uint32_t* whist = area + w * kWideBins;  // [kTopkWarps][kWideBins] over the staging area
+  for (int i = tid; i < kTopkWarps * kWideBins; i += kTopkThreads) area[i] = 0;
+  __syncthreads();
+  // segments of whole float4 groups (rows start 16-byte aligned)
+  const int n4 = (n + 3) / 4;
+  const int seg4 = (n4 + kTopkWarps - 1) / kTopkWarps;
+  const int s0 = min(n4, w * seg4), s1 = min(n4, s0 + seg4);
+  const float4* g4 = reinterpret_cast<const float4*>(g);
+  constexpr int U = 8;  // float4 loads in flight per lane
+  // ---- A
+  for (int b = s0; b < s1; b += 32 * U) {
+    float4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i4 = b + u * 32 + lane;
+      v[u] = i4 < s1 ? __ldg(g4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = 4 * (b + u * 32 + lane);
+      const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (i + c < n && i < 4 * s1) atomicAdd(whist + (ordered_key(e[c]) >> kWideShift), 1u);
+    }
+  }
+  __syncthreads();
+  // bin totals, scanned from the top bin down: thread tid owns bins
+  // 2047 - 4*tid .. 2044 - 4*tid
+  uint32_t cnt[4], tot = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int bin = kWideBins - 1 - (4 * tid + j);
+    uint32_t c = 0;
+#pragma unroll 4
+    for (int ww = 0; ww < kTopkWarps; ++ww) c += area[ww * kWideBins + bin];
+    cnt[j] = c;
+    tot += c;
+  }
+  // block-wide exclusive scan of the per-thread totals
+  uint32_t x = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_tmp[w] = (int)x;
+  __syncthreads();
+  if (w == 0) {
+    uint32_t y = lane < kTopkWarps ? (uint32_t)s_tmp[lane] : 0u;
+    const uint32_t orig = y;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t z = __shfl_up_sync(0xffffffffu, y, o);
+      if (lane >= o) y += z;
+    }
+    if (lane < kTopkWarps) s_tmp[32 + lane] = (int)(y - orig);
+  }
+  __syncthreads();
+  uint32_t above = (uint32_t)s_tmp[32 + w] + (x - tot);  // keys in bins above this thread's first bin
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (above < (uint32_t)k && above + cnt[j] >= (uint32_t)k) {
+      s_sel[0] = kWideBins - 1 - (4 * tid + j);
+      s_sel[1] = (int)(above + cnt[j]);  // candidates: keys in bins >= b*
+    }
+    above += cnt[j];
+  }
+  __syncthreads();
+  const int bstar = s_sel[0];
+  const int m = s_sel[1];
+  if (m > kCandCap) return false;  // uniform over the block
+  // per-warp candidate counts (suffix sums of the warp's own histogram) and offsets
+  uint32_t mine = 0;
+  for (int bin = bstar + lane; bin < kWideBins; bin += 32) mine += whist[bin];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+  if (lane == 0) s_woff[w] = (int)mine;
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int ww = 0; ww < kTopkWarps; ++ww) {
+      const int c = s_woff[ww];
+      s_woff[ww] = acc;
+      acc += c;
+    }
+    s_woff[kTopkWarps] = acc;
+  }
+  __syncthreads();  // the histograms are dead from here on: the area holds the list
+  uint32_t* ckey = area;
+  int* cidx = reinterpret_cast<int*>(area + kCandCap);
+  // ---- B: ordered compaction of this warp's segment
+  int run = s_woff[w];
+  for (int b = s0; b < s1; b += 32 * U) {
+    float4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i4 = b + u * 32 + lane;
+      v[u] = i4 < s1 ? __ldg(g4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = 4 * (b + u * 32 + lane);
+      const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      uint32_t key[4];
+      int c = 0;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        key[cc] = ordered_key(e[cc]);
+        const bool in = i + cc < n && i < 4 * s1 && (int)(key[cc] >> kWideShift) >= bstar;
+        c += in ? 1 : 0;
+      }
+      // lanes hold consecutive groups of four positions: an exclusive scan of
+      // the per-lane counts keeps the list in position order
+      int xs = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, xs, o);
+        if (lane >= o) xs += y;
+      }
+      int pos = run + xs - c;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const bool in = i + cc < n && i < 4 * s1 && (int)(key[cc] >> kWideShift) >= bstar;
+        if (in) {
+          ckey[pos] = key[cc];
+          cidx[pos] = i + cc;
+          ++pos;
+        }
+      }
+      run += __shfl_sync(0xffffffffu, xs, 31);
+    }
+  }
+  __syncthreads();
+  // ---- C: exact radix select of rank k among the m candidates
+  uint32_t prefix = 0, mask = 0;
+  int remaining = k;
+  const int mround = (m + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = tid; i < kTopkWarps * 256; i += kTopkThreads) hist[i] = 0;
+    __syncthreads();
+    uint32_t* wh = hist + w * 256;
+    for (int i = tid; i < mround; i += kTopkThreads) hist_add(wh, i < m ? ckey[i] : 0u, i < m, prefix, mask, shift);
+    __syncthreads();
+    pick_digit(hist, shift, prefix, mask, remaining, s_sel);
+  }
+  emit_ordered<true>(g, ckey, m, prefix, remaining, out_idx, out_val, s_tmp, cidx);
+  return true;
+}
+
 // Row staged in shared memory as ordered keys; the histograms of the first
 // pass (top digit) were counted while staging.
 __device__ void select_row_staged(const float* __restrict__ g, const uint32_t* __restrict__ s_row, int n, int k,
@@ -350,13 +528,17 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const float* __
     __syncthreads();
     select_row_staged(g, s_row, n, k, oi, ov, hist, s_tmp);
   } else {
-    select_row_global(g, n, k, oi, ov, hist, s_tmp, reinterpret_cast<int*>(s_row), cap / 2);
+    if (cap < kTopkSmemCap || !select_row_two_pass(g, n, k, oi, ov, hist, s_row, s_tmp))
+      select_row_global(g, n, k, oi, ov, hist, s_tmp, reinterpret_cast<int*>(s_row), cap / 2);
   }
 }
 
 int run_topk(cudaStream_t stream, const float* scores, long long ld, const int* nvis, int T, int div, int k,
              int32_t* out_idx, float* out_val, int max_len) {
   if (T == 0) return DSA_OK;
+  // rows longer than the staging capacity are read as float4: every row must
+  // start 16-byte aligned
+  if ((ld & 3) || (reinterpret_cast<uintptr_t>(scores) & 15)) return DSA_ERR_ALIGNMENT;
   // rows longer than the staging capacity use the staging area as two
   // winner lists of cap/2 entries each
   const int cap = max_len > kTopkSmemCap ? kTopkSmemCap : max(0, max_len);

@@ -57,3 +57,23 @@ def test_long_rows_token_topk(dsa):
     assert np.array_equal(got[2], np.arange(wl.k))
     # the 4-value row: the winners are exact (no near-tie freedom between distinct values)
     assert np.array_equal(got[1], ref[1])
+
+
+def test_long_rows_k_above_the_winner_lists(dsa):
+    """k larger than the shared-memory candidate and winner lists (half the
+    staging area each): the winners are emitted in position order straight
+    from the score row."""
+    dev = torch.device("cuda")
+    wl = _long_workload()
+    rg = wl.rg
+    k = 20000
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    topk = dsa.dsa_indexer_topk(wl.q_idx.to(dev), wl.w.to(dev), wl.kcache[0].to(dev), *meta_to(rg, dev), k=k,
+                                max_kv=rg.max_kv, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    rows = O.indexer_scores(f32(wl.q_idx), f32(wl.w), f32(wl.kcache[0]), **meta_np(rg))
+    ref = O.topk_rows_of(rows, k)
+    got = topk.cpu().numpy()
+    check_topk_rows(got, ref, k, rows)
+    assert np.array_equal(got[2], np.arange(k))  # the all-tie row: the lowest k positions
