@@ -34,10 +34,13 @@
 namespace dsa {
 
 namespace {
-// warp 0 MMA, warp 1 key generator, warps 2-3 and 8-11 gather, warps 4-7 softmax
-constexpr int kThreads = 384;
-constexpr int kCopyWarps = 6;
-constexpr int kCopyThreads = kCopyWarps * 32;
+// warp 0 MMA, warp 1 key generator, warps 2-3 and 8.. gather, warps 4-7 softmax.
+// Scattered token rows are copied by ten warps (512 threads: more copies in
+// flight, measured 10% faster decode than six); the page-run modes, whose
+// steps are single TMA boxes, run with six (384 threads) in an instantiation
+// of their own.
+constexpr int kCopyWarpsToken = 10;
+constexpr int kCopyWarpsRuns = 6;
 constexpr int kSubKeys = 32;   // keys resolved / copied per generator step
 constexpr int kTileKeys = 64;  // keys per MMA tile (two generator steps)
 constexpr int kRing = 12;      // generator steps buffered ahead of the gather
@@ -79,7 +82,7 @@ constexpr int OFF_WTS = OFF_STAGE + 128 * kStageLd * 4;  // fp32 merge weights [
 static_assert(OFF_WTS + kMaxSplits * 128 * 4 <= OFF_VST, "the stage must stay clear of the value stages");
 // every full barrier completes after two generator steps' worth of arrivals:
 // each gather thread once per step, plus one more by the leader per step
-constexpr uint32_t kFullArrivals = 2 * (kCopyThreads + 1);
+__device__ __forceinline__ uint32_t full_arrivals(int copy_threads) { return 2u * (uint32_t)(copy_threads + 1); }
 
 }  // namespace
 
@@ -355,8 +358,10 @@ __device__ __forceinline__ void mma_issuer(uint32_t tmem, uint32_t qs_addr, uint
 
 // kSoftCap: the logit cap of the dense fallback, a separate instantiation
 // so that the common path carries none of its code
-template <bool kSoftCap>
-__global__ void __launch_bounds__(kThreads, 1)
+// kCopyW: copier warps (kCopyWarpsToken or kCopyWarpsRuns); the block has
+// (6 + kCopyW) warps
+template <bool kSoftCap, int kCopyW>
+__global__ void __launch_bounds__((6 + kCopyW) * 32, 1)
     sparse_mla_kernel(const AttendParams prm, const __grid_constant__ CUtensorMap kvmap,
                       const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -365,6 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   const int warp = warp_id(), lane = lane_id(), tid = threadIdx.x;
+  constexpr int n_copy_warps = kCopyW;
+  constexpr int n_copy_threads = n_copy_warps * 32;
   const int half = blockIdx.x & 1, hg = blockIdx.x >> 1;
   const int t = blockIdx.y, split = blockIdx.z;
   const int h0 = hg * 128;
@@ -379,9 +386,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile uint32_t* vst_mask = kst_end + kKStages;   // [kVStages][2]
   volatile uint32_t* vst_end = vst_mask + 2 * kVStages;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint64_t* kfull = bars;                 // [kKStages] kFullArrivals + tx bytes
+  uint64_t* kfull = bars;                 // [kKStages] full_arrivals + tx bytes
   uint64_t* kempty = kfull + kKStages;    // [kKStages] commit after the K-part MMAs
-  uint64_t* vfull = kempty + kKStages;    // [kVStages] kFullArrivals + tx bytes
+  uint64_t* vfull = kempty + kKStages;    // [kVStages] full_arrivals + tx bytes
   uint64_t* vempty = vfull + kVStages;    // [kVStages] commit after PV
   uint64_t* rfull = vempty + kVStages;    // [kRing] generator
   uint64_t* rempty = rfull + kRing;       // [kRing] gather threads
@@ -395,16 +402,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < kKStages; ++i) {
-      mbar_init(kfull + i, kFullArrivals);
+      mbar_init(kfull + i, full_arrivals(n_copy_threads));
       mbar_init(kempty + i, 1);
     }
     for (int i = 0; i < kVStages; ++i) {
-      mbar_init(vfull + i, kFullArrivals);
+      mbar_init(vfull + i, full_arrivals(n_copy_threads));
       mbar_init(vempty + i, 1);
     }
     for (int i = 0; i < kRing; ++i) {
       mbar_init(rfull + i, 1);
-      mbar_init(rempty + i, kCopyThreads);
+      mbar_init(rempty + i, n_copy_threads);
     }
     mbar_init(sfull, 1);
     mbar_init(sfull + 1, 1);
@@ -533,9 +540,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Tile by tile (two generator steps): the K parts of both steps as soon
     // as the K stage is free, then the V parts once PV has released the V
     // stage, so a K part is never held up behind the V stage.
-    const int cw = warp < 4 ? warp - 2 : warp - 6;  // 0..5
+    const int cw = warp < 4 ? warp - 2 : warp - 6;  // 0 .. n_copy_warps - 1
     const int ctid = cw * 32 + lane;
-    // scattered rows: copier warp cw copies keys cw, cw+6, ... of a step; per
+    // scattered rows: copier warp cw copies keys cw, cw+n, ... of a step; per
     // key the K part is 40 16-byte chunks (lanes 0..31, then 0..7 again) and
     // the V part 32 (one per lane), each a contiguous run of the row
     const int kc1 = lane + 32;
@@ -593,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
 #pragma unroll 2
-          for (int key = cw; key < kSubKeys; key += kCopyWarps) {
+          for (int key = cw; key < kSubKeys; key += n_copy_warps) {
             const int r = ring_rows[slot * 32 + key];
             const uint16_t* rb = r >= 0 ? prm.kv + (size_t)r * prm.row_stride : prm.kv;
             const uint32_t nb = r >= 0 ? 16u : 0u;
@@ -627,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
 #pragma unroll 2
-          for (int key = cw; key < kSubKeys; key += kCopyWarps) {
+          for (int key = cw; key < kSubKeys; key += n_copy_warps) {
             const int r = ring_rows[slot * 32 + key];
             const uint16_t* rb = r >= 0 ? prm.kv + (size_t)r * prm.row_stride : prm.kv;
             cp_async16(d + dst_v + sw128_offset(key, lane & 7), rb + src_v, r >= 0 ? 16u : 0u);
@@ -971,12 +978,16 @@ int run_attend(cudaStream_t stream, AttendParams prm, void* ws, size_t ws_bytes)
     return DSA_ERR_CUDA;
   if (!encode_bf16_2d(&qmap, prm.q, (uint64_t)prm.T * prm.H, kDk, 128, kDk)) return DSA_ERR_CUDA;
   dim3 grid(cols, prm.T, prm.nsplit);
-  if (prm.soft_cap_on) {
-    set_smem_attr_once(reinterpret_cast<const void*>(sparse_mla_kernel<true>), kSmem);
-    sparse_mla_kernel<true><<<grid, kThreads, kSmem, stream>>>(prm, kvmap, qmap);
+  if (prm.soft_cap_on) {  // dense mode only: page runs
+    set_smem_attr_once(reinterpret_cast<const void*>(sparse_mla_kernel<true, kCopyWarpsRuns>), kSmem);
+    sparse_mla_kernel<true, kCopyWarpsRuns><<<grid, (6 + kCopyWarpsRuns) * 32, kSmem, stream>>>(prm, kvmap, qmap);
+  } else if (prm.mode == kModeToken) {
+    set_smem_attr_once(reinterpret_cast<const void*>(sparse_mla_kernel<false, kCopyWarpsToken>), kSmem);
+    sparse_mla_kernel<false, kCopyWarpsToken><<<grid, (6 + kCopyWarpsToken) * 32, kSmem, stream>>>(prm, kvmap,
+                                                                                                   qmap);
   } else {
-    set_smem_attr_once(reinterpret_cast<const void*>(sparse_mla_kernel<false>), kSmem);
-    sparse_mla_kernel<false><<<grid, kThreads, kSmem, stream>>>(prm, kvmap, qmap);
+    set_smem_attr_once(reinterpret_cast<const void*>(sparse_mla_kernel<false, kCopyWarpsRuns>), kSmem);
+    sparse_mla_kernel<false, kCopyWarpsRuns><<<grid, (6 + kCopyWarpsRuns) * 32, kSmem, stream>>>(prm, kvmap, qmap);
   }
   DSA_CHECK_LAUNCH();
   return DSA_OK;
