@@ -248,24 +248,13 @@ def stage_roofline(wl, rn, timed, extras=True):
         out["sparse_mla_decode"] = entry(timed(lambda: rn.attend(0)), 1152 * keys, "hbm", n_layers)
     if not extras:
         return out
-    # the step before the path: paged write-back of every query token's
-    # latent row and indexer key (the rows already there are written back
-    # unchanged, so the caches keep their contents): 2 x (576 + 128) x 2 B per
-    # token, read and written
+    # the first stage of every layer: paged write-back of the new tokens'
+    # latent rows and (full layers) indexer keys (the synthetic caches already
+    # hold these rows, so they are written back unchanged): 2 x (576 + 128) x
+    # 2 B per token, read and written, on a full layer
     import deepseek_sparse_attention_score_gb300 as dsa
 
-    tseq, tpos = rg.token_seq(), rg.token_pos()
-    ent = rg.cu_kv_lens[tseq] // ps + tpos // ps
-    phys = torch.from_numpy((rg.page_indices[ent].astype(np.int64) * ps + tpos % ps)).to(rn.kv[0].device)
-    kv_rows = rn.kv[0].view(-1, rn.kv[0].shape[-1]).index_select(0, phys)[:, :576].contiguous()
-    k_rows = rn.kcache[0].view(-1, 128).index_select(0, phys).contiguous()
-
-    def write_back():
-        dsa.dsa_paged_write_back(kv_rows, rn.kv[0], *rn.meta, D=576, dev_status=rn.status)
-        dsa.dsa_paged_write_back(k_rows, rn.kcache[0], *rn.meta, D=128, dev_status=rn.status)
-
-    out["paged_write_back"] = entry(timed(write_back), 2 * (576 + 128) * 2 * rg.T, "hbm")
-    out["paged_write_back"]["in_step"] = False
+    out["paged_write_back"] = entry(timed(lambda: rn.write_back(0)), 2 * (576 + 128) * 2 * rg.T, "hbm", n_layers)
     # the dense fallback (layers without an indexer) over the same queries:
     # every visible position, 1152 B (decode, HBM) or 2*H*(576+512) FLOP
     # (prefill, tensor) per visible (query, key) pair; timed beside the step
@@ -666,15 +655,17 @@ def run_ours(args):
     h_q_idx, h_w = pin(rn.q_idx), pin(rn.w)
     h_q = [pin(x) for x in rn.q]
     h_meta = [pin(m) for m in rn.meta]
+    h_new_kv = [pin(x) for x in rn.new_kv]
+    h_new_k = [pin(x) for x in rn.new_k]
     h_topk = torch.empty(rn.topk[0].shape, dtype=torch.int32).pin_memory()
     h_o = [torch.empty(x.shape, dtype=torch.bfloat16).pin_memory() for x in rn.o]
-    h2d = sum(t.numel() * t.element_size() for t in [h_q_idx, h_w, *h_q, *h_meta])
+    h2d = sum(t.numel() * t.element_size() for t in [h_q_idx, h_w, *h_q, *h_meta, *h_new_kv, *h_new_k])
     d2h = h_topk.numel() * 4 + sum(x.numel() * 2 for x in h_o)
 
     # the whole host-buffer step (copies on two streams, kernels) as one
     # CUDA graph; every replay copies the inputs in and the outputs out
     side = torch.cuda.Stream(dev)
-    e2e_eager = lambda: rn.step_host(h_q_idx, h_w, h_q, h_meta, h_topk, h_o, side)
+    e2e_eager = lambda: rn.step_host(h_q_idx, h_w, h_q, h_meta, h_topk, h_o, side, h_new_kv, h_new_k)
     e2e_step, e2e_graph = e2e_eager, False
     try:
         s2 = torch.cuda.Stream(dev)
@@ -710,7 +701,7 @@ def run_ours(args):
               "l2": "flushed (512 MB write) before every timed step", "cuda_graph": graph is not None,
               "parallelism": "replicas" if world > 1 else "single"}
     # free the headline workload before the side workloads are built
-    del rn, wl, graph, h_q, h_o, h_q_idx, h_w, h_meta, h_topk
+    del rn, wl, graph, h_q, h_o, h_q_idx, h_w, h_meta, h_topk, h_new_kv, h_new_k
     torch.cuda.empty_cache()
     sides = {}
     if not args.only and rank == 0 and world == 1:

@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(kBinThreads) approx_bins_kernel(const float* _
                                                                   const int* __restrict__ nvis, int kb,
                                                                   float* __restrict__ vals, int* __restrict__ pos,
                                                                   int* __restrict__ nb, long long ldb) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int t = blockIdx.x;
   const int n = nvis[t];
   const int B = min(n, kb);
@@ -48,6 +50,8 @@ __global__ void __launch_bounds__(kBinThreads) approx_bins_kernel(const float* _
 __global__ void __launch_bounds__(kFinThreads) approx_finish_kernel(const int32_t* __restrict__ cand, int k,
                                                                     const int* __restrict__ pos, long long ldb,
                                                                     int32_t* __restrict__ out, int n_pow2) {
+  griddep_launch_dependents();
+  griddep_wait();
   extern __shared__ int a[];
   const int t = blockIdx.x;
   for (int i = threadIdx.x; i < n_pow2; i += kFinThreads) {
@@ -83,16 +87,16 @@ int run_topk_approx(cudaStream_t stream, const float* scores, long long ld, cons
   const int bmax = (int)(kb < max_kv ? kb : max_kv);
   const int ldb = (bmax + 3) & ~3;  // bin rows start 16-byte aligned (the top-k reads them as float4)
   dim3 g1(T, (bmax + kBinThreads - 1) / kBinThreads);
-  approx_bins_kernel<<<g1, kBinThreads, 0, stream>>>(scores, ld, nvis, (int)(kb < (1LL << 30) ? kb : (1LL << 30)),
+  DSA_LAUNCH_PDL(approx_bins_kernel, dim3(g1), dim3(kBinThreads), 0, stream, scores, ld, nvis,
+                 (int)(kb < (1LL << 30) ? kb : (1LL << 30)),
                                                      vals, pos, nb, ldb);
-  DSA_CHECK_LAUNCH();
   int rc = run_topk(stream, vals, ldb, nb, T, 1, k, cand, nullptr, bmax);
   if (rc) return rc;
   int n_pow2 = 1;
   while (n_pow2 < k) n_pow2 <<= 1;
   set_smem_attr_once(reinterpret_cast<const void*>(approx_finish_kernel), approx_max_k() * 4);
-  approx_finish_kernel<<<T, kFinThreads, (size_t)n_pow2 * 4, stream>>>(cand, k, pos, ldb, out, n_pow2);
-  DSA_CHECK_LAUNCH();
+  DSA_LAUNCH_PDL(approx_finish_kernel, dim3(T), dim3(kFinThreads), (size_t)n_pow2 * 4, stream, cand, k, pos, ldb,
+                 out, n_pow2);
   return DSA_OK;
 }
 

@@ -369,6 +369,7 @@ __global__ void __launch_bounds__((6 + kCopyW) * 32, 1)
     if (threadIdx.x == 0) set_status(prm.dev_status, DSA_STATUS_INTERNAL);
     return;
   }
+  griddep_launch_dependents();
   const int warp = warp_id(), lane = lane_id(), tid = threadIdx.x;
   constexpr int n_copy_warps = kCopyW;
   constexpr int n_copy_threads = n_copy_warps * 32;
@@ -429,6 +430,9 @@ __global__ void __launch_bounds__((6 + kCopyW) * 32, 1)
   }
   // barrier initialisation must be visible before the Q copy signals one
   __syncthreads();
+  // the local set-up above overlaps the previous kernel of the stream; global
+  // memory is touched only after it has completed
+  griddep_wait();
   // Q rows h0..h0+127 of token t (rows past H belong to the next token or
   // lie past the tensor, where TMA fills zeros; their outputs are never
   // stored) as nine 128-byte-swizzled column blocks: Q[:, 256:576] stays in
@@ -978,18 +982,20 @@ int run_attend(cudaStream_t stream, AttendParams prm, void* ws, size_t ws_bytes)
     return DSA_ERR_CUDA;
   if (!encode_bf16_2d(&qmap, prm.q, (uint64_t)prm.T * prm.H, kDk, 128, kDk)) return DSA_ERR_CUDA;
   dim3 grid(cols, prm.T, prm.nsplit);
+  void (*kern)(AttendParams, CUtensorMap, CUtensorMap);
+  int threads;
   if (prm.soft_cap_on) {  // dense mode only: page runs
-    set_smem_attr_once(reinterpret_cast<const void*>(sparse_mla_kernel<true, kCopyWarpsRuns>), kSmem);
-    sparse_mla_kernel<true, kCopyWarpsRuns><<<grid, (6 + kCopyWarpsRuns) * 32, kSmem, stream>>>(prm, kvmap, qmap);
+    kern = sparse_mla_kernel<true, kCopyWarpsRuns>;
+    threads = (6 + kCopyWarpsRuns) * 32;
   } else if (prm.mode == kModeToken) {
-    set_smem_attr_once(reinterpret_cast<const void*>(sparse_mla_kernel<false, kCopyWarpsToken>), kSmem);
-    sparse_mla_kernel<false, kCopyWarpsToken><<<grid, (6 + kCopyWarpsToken) * 32, kSmem, stream>>>(prm, kvmap,
-                                                                                                   qmap);
+    kern = sparse_mla_kernel<false, kCopyWarpsToken>;
+    threads = (6 + kCopyWarpsToken) * 32;
   } else {
-    set_smem_attr_once(reinterpret_cast<const void*>(sparse_mla_kernel<false, kCopyWarpsRuns>), kSmem);
-    sparse_mla_kernel<false, kCopyWarpsRuns><<<grid, (6 + kCopyWarpsRuns) * 32, kSmem, stream>>>(prm, kvmap, qmap);
+    kern = sparse_mla_kernel<false, kCopyWarpsRuns>;
+    threads = (6 + kCopyWarpsRuns) * 32;
   }
-  DSA_CHECK_LAUNCH();
+  set_smem_attr_once(reinterpret_cast<const void*>(kern), kSmem);
+  DSA_LAUNCH_PDL(kern, grid, dim3(threads), kSmem, stream, prm, kvmap, qmap);
   return DSA_OK;
 }
 

@@ -87,6 +87,29 @@ void note_launch();  // process-wide count of enqueued kernels
     ::dsa::note_launch();                               \
   } while (0)
 
+// Launch with programmatic stream serialization (the kernel may start while
+// the previous kernel of the stream is finishing; it waits for it with
+// griddep_wait before touching global memory), turning a launch error into
+// DSA_ERR_CUDA and counting the launch.
+#define DSA_LAUNCH_PDL(kernel, grid, block, smem, stream, ...)                        \
+  do {                                                                                \
+    cudaLaunchConfig_t cfg_ = {};                                                     \
+    cfg_.gridDim = (grid);                                                            \
+    cfg_.blockDim = (block);                                                          \
+    cfg_.dynamicSmemBytes = (smem);                                                   \
+    cfg_.stream = (stream);                                                           \
+    cudaLaunchAttribute attr_[1];                                                     \
+    attr_[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;                 \
+    attr_[0].val.programmaticStreamSerializationAllowed = 1;                          \
+    cfg_.attrs = attr_;                                                               \
+    cfg_.numAttrs = 1;                                                                \
+    if (cudaLaunchKernelEx(&cfg_, kernel, __VA_ARGS__) != cudaSuccess) {              \
+      (void)cudaGetLastError();                                                       \
+      return DSA_ERR_CUDA;                                                            \
+    }                                                                                 \
+    ::dsa::note_launch();                                                             \
+  } while (0)
+
 namespace dsa {
 int sm_count();  // cached per device
 // Raise a kernel's dynamic shared-memory limit once per device (not during

@@ -47,6 +47,8 @@ __device__ int block_excl_scan(int v, int* s_warp, int* total) {
 constexpr int kPlanStageS = 4096;  // requests whose query offsets the planner keeps in shared memory
 
 __global__ void __launch_bounds__(1024) indexer_plan_kernel(IndexerMeta m, IndexerPlan pl, int ch1, int ch8) {
+  griddep_launch_dependents();
+  griddep_wait();
   __shared__ int s_warp[32];
   __shared__ int s_cuq[kPlanStageS + 1];
   __shared__ int s_off[1024];
@@ -199,6 +201,8 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::THREADS, 1)
                          const __grid_constant__ CUtensorMap qmap) {
   using C = IdxCfg<NQ>;
   extern __shared__ __align__(1024) uint8_t smem[];
+  griddep_launch_dependents();
+  griddep_wait();
   const int n_items = NQ == 1 ? pl.counts[0] : pl.counts[1];
   if ((int)blockIdx.x >= n_items) return;
   const int4* items = NQ == 1 ? pl.dec_items : pl.pre_items;
@@ -522,20 +526,17 @@ int run_indexer(cudaStream_t stream, const IndexerMeta& m, const uint16_t* q, co
   CUtensorMap qmap8;
   if (!encode_bf16_2d(&qmap8, q, (uint64_t)m.T * 32, 128, 256, 128)) return DSA_ERR_CUDA;
 
-  indexer_plan_kernel<<<1, 1024, 0, stream>>>(m, pl, kChunkDecode, kChunkPrefill);
-  DSA_CHECK_LAUNCH();
+  DSA_LAUNCH_PDL(indexer_plan_kernel, dim3(1), dim3(1024), 0, stream, m, pl, kChunkDecode, kChunkPrefill);
   const int sms = sm_count();
   {
     using C = IdxCfg<1>;
     set_smem_attr_once(reinterpret_cast<const void*>(indexer_score_kernel<1>), C::SMEM);
-    indexer_score_kernel<1><<<sms, C::THREADS, C::SMEM, stream>>>(m, pl, out, kmap, qmap);
-    DSA_CHECK_LAUNCH();
+    DSA_LAUNCH_PDL(indexer_score_kernel<1>, dim3(sms), dim3(C::THREADS), C::SMEM, stream, m, pl, out, kmap, qmap);
   }
   {
     using C = IdxCfg<8>;
     set_smem_attr_once(reinterpret_cast<const void*>(indexer_score_kernel<8>), C::SMEM);
-    indexer_score_kernel<8><<<sms, C::THREADS, C::SMEM, stream>>>(m, pl, out, kmap, qmap8);
-    DSA_CHECK_LAUNCH();
+    DSA_LAUNCH_PDL(indexer_score_kernel<8>, dim3(sms), dim3(C::THREADS), C::SMEM, stream, m, pl, out, kmap, qmap8);
   }
   return DSA_OK;
 }

@@ -17,6 +17,8 @@ constexpr int kPgWarps = kPgThreads / 32;
 __global__ void __launch_bounds__(kPgThreads) topk_pages_kernel(const int32_t* __restrict__ topk, int K, int ps,
                                                                 int max_pages, int cap, int32_t* __restrict__ pages,
                                                                 int32_t* __restrict__ counts, int32_t* dev_status) {
+  griddep_launch_dependents();
+  griddep_wait();
   extern __shared__ uint32_t bm[];
   __shared__ int s_warp[kPgWarps + 1];
   const int row = blockIdx.x, tid = threadIdx.x, lane = lane_id(), w = warp_id();
@@ -86,8 +88,8 @@ int run_topk_pages(cudaStream_t stream, const int32_t* topk, int T, int K, int p
   if (T == 0) return DSA_OK;
   const size_t smem = topk_pages_smem(max_pages);
   set_smem_attr_once(reinterpret_cast<const void*>(topk_pages_kernel), (int)topk_pages_smem(kTopkPagesMaxPages));
-  topk_pages_kernel<<<T, kPgThreads, smem, stream>>>(topk, K, ps, max_pages, cap, pages, counts, dev_status);
-  DSA_CHECK_LAUNCH();
+  DSA_LAUNCH_PDL(topk_pages_kernel, dim3(T), dim3(kPgThreads), smem, stream, topk, K, ps, max_pages, cap, pages,
+                 counts, dev_status);
   return DSA_OK;
 }
 

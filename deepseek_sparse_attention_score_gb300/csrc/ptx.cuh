@@ -294,6 +294,17 @@ __device__ __forceinline__ float warp_max_f32(float v) {
   return r;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel of the stream finishes.
+// griddep_launch_dependents lets the next kernel of the stream start early;
+// griddep_wait blocks until every earlier kernel of the stream has completed
+// and its memory is visible. Every kernel of this library waits before it
+// touches global memory.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ int warp_id() { return threadIdx.x >> 5; }
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 __device__ __forceinline__ bool elect_one() {

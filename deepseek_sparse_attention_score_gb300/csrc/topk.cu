@@ -485,6 +485,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const float* __
                                                                  const int* __restrict__ nvis, int div, int k,
                                                                  int32_t* __restrict__ out_idx,
                                                                  float* __restrict__ out_val, int cap) {
+  griddep_launch_dependents();
+  griddep_wait();
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int s_tmp[72];
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem);  // (warps + 1) * 256
@@ -544,8 +546,8 @@ int run_topk(cudaStream_t stream, const float* scores, long long ld, const int* 
   const int cap = max_len > kTopkSmemCap ? kTopkSmemCap : max(0, max_len);
   const size_t smem = (size_t)(kTopkWarps + 1) * 256 * 4 + (size_t)cap * 4;
   set_smem_attr_once(reinterpret_cast<const void*>(topk_rows_kernel), (int)(kTopkSmemMax));
-  topk_rows_kernel<<<T, kTopkThreads, smem, stream>>>(scores, ld, nvis, div, k, out_idx, out_val, cap);
-  DSA_CHECK_LAUNCH();
+  DSA_LAUNCH_PDL(topk_rows_kernel, dim3(T), dim3(kTopkThreads), smem, stream, scores, ld, nvis, div, k, out_idx,
+                 out_val, cap);
   return DSA_OK;
 }
 

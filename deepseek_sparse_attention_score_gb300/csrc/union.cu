@@ -34,6 +34,8 @@ __global__ void __launch_bounds__(kUnionThreads) block_union_kernel(const int32_
                                                                     uint32_t* __restrict__ member,
                                                                     int32_t* __restrict__ counts,
                                                                     int32_t* dev_status) {
+  griddep_launch_dependents();
+  griddep_wait();
   __shared__ uint32_t bits[kWindowWords];
   __shared__ int s_base[kUnionThreads];
   __shared__ int s_warp[32];
@@ -145,9 +147,8 @@ int run_block_union(cudaStream_t stream, const int32_t* topk_units, int T, int K
                     uint32_t* member, int32_t* counts, int32_t* dev_status) {
   const int nqb = (T + QB - 1) / QB;
   if (nqb == 0) return DSA_OK;
-  block_union_kernel<<<nqb, kUnionThreads, 0, stream>>>(topk_units, T, K, QB, u_max, cu_q_lens, cu_kv_lens, S, ps,
-                                                         PTW, units, member, counts, dev_status);
-  DSA_CHECK_LAUNCH();
+  DSA_LAUNCH_PDL(block_union_kernel, dim3(nqb), dim3(kUnionThreads), 0, stream, topk_units, T, K, QB, u_max,
+                 cu_q_lens, cu_kv_lens, S, ps, PTW, units, member, counts, dev_status);
   return DSA_OK;
 }
 

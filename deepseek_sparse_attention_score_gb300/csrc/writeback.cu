@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(kWbThreads) paged_write_back_kernel(
     long long cache_stride, const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q_lens,
     const int32_t* __restrict__ cu_kv_lens, const int32_t* __restrict__ page_indices, int T, int S, int P, int PTW,
     int ps, int32_t* dev_status) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int lane = lane_id();
   const int t = blockIdx.x * (kWbThreads / 32) + warp_id();
   if (t >= T) return;
@@ -50,10 +52,8 @@ int run_paged_write_back(cudaStream_t stream, const uint16_t* rows, long long sr
                          int ps, int32_t* dev_status) {
   if (T == 0) return DSA_OK;
   const int per = kWbThreads / 32;
-  paged_write_back_kernel<<<(T + per - 1) / per, kWbThreads, 0, stream>>>(
-      rows, src_stride, D, cache, cache_stride, seq_lens, cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps,
-      dev_status);
-  DSA_CHECK_LAUNCH();
+  DSA_LAUNCH_PDL(paged_write_back_kernel, dim3((T + per - 1) / per), dim3(kWbThreads), 0, stream, rows, src_stride,
+                 D, cache, cache_stride, seq_lens, cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps, dev_status);
   return DSA_OK;
 }
 

@@ -1,11 +1,14 @@
 """One DSA layer step on a resident batch, built from the C-ABI calls.
 
-Decode batches run indexer -> token top-k (or page top-k with a page budget)
--> sparse MLA decode. Prefill / mixed batches run, on full layers, the
-indexer once for both the page top-k (K_p = ceil(k/ps), what the attention
-consumes) and the token top-k, then the block union and the query-block
-sparse MLA; shared layers (IndexShare, ref.py build_index_share_map) reuse the
-top-k and union tables of their source slot and run the attention only.
+Every layer first writes its new tokens' rows into the paged caches (the
+latent row of every layer, the indexer key on full layers; the backend's
+_scatter_paged step that precedes the path). Decode batches then run indexer
+-> token top-k (or page top-k with a page budget) -> sparse MLA decode.
+Prefill / mixed batches run, on full layers, the indexer once for both the
+page top-k (K_p = ceil(k/ps), what the attention consumes) and the token
+top-k, then the block union and the query-block sparse MLA; shared layers
+(IndexShare, ref.py build_index_share_map) reuse the top-k and union tables of
+their source slot and run the attention only.
 
 All buffers are allocated once up front, so a step only enqueues kernels and
 can be captured in a CUDA graph.
@@ -43,6 +46,14 @@ class LayerRunner:
         self.kv = [x.to(dev) for x in wl.kv]
         self.types = list(wl.indexer_types) if wl.indexer_types else [0]
         self.full_slot, self.src_slot, self.num_full = abi.dsa_index_build_share_map(self.types, len(self.types))
+        # the new tokens' rows (latent rows per layer, indexer keys per full
+        # slot): taken from the synthetic caches, which already hold them, so
+        # writing them back leaves every cache as generated
+        tseq, tpos = rg.token_seq(), rg.token_pos()
+        ent = rg.cu_kv_lens[tseq] // rg.page_size + tpos // rg.page_size
+        rows = torch.from_numpy(rg.page_indices[ent].astype("int64") * rg.page_size + tpos % rg.page_size).to(dev)
+        self.new_kv = [c.view(-1, c.shape[-1]).index_select(0, rows)[:, :576].contiguous() for c in self.kv]
+        self.new_k = [c.view(-1, c.shape[-1]).index_select(0, rows).contiguous() for c in self.kcache]
         T, H = self.T, wl.H
         self.H = H
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -65,6 +76,14 @@ class LayerRunner:
             self.counts = [torch.empty((nqb,), dtype=torch.int32, device=dev) for _ in range(self.num_full)]
 
     # -- stages ---------------------------------------------------------------
+    def write_back(self, layer):
+        """The layer's new latent rows, and on a full layer its new indexer
+        keys, into their slots of the paged caches."""
+        abi.dsa_paged_write_back(self.new_kv[layer], self.kv[layer], *self.meta, D=576, dev_status=self.status)
+        if self.full_slot[layer] >= 0:
+            slot = self.full_slot[layer]
+            abi.dsa_paged_write_back(self.new_k[slot], self.kcache[slot], *self.meta, D=128, dev_status=self.status)
+
     def index(self, slot):
         if self.prefill or self.page_budget is not None:
             abi.dsa_indexer_page_topk(self.q_idx, self.w, self.kcache[slot], *self.meta, k_pages=self.k_pages,
@@ -96,6 +115,7 @@ class LayerRunner:
                                       dev_status=self.status)
 
     def layer_step(self, layer):
+        self.write_back(layer)
         if self.full_slot[layer] >= 0:
             slot = self.full_slot[layer]
             self.index(slot)
@@ -108,13 +128,14 @@ class LayerRunner:
         for layer in range(len(self.types)):
             self.layer_step(layer)
 
-    def step_host(self, h_q_idx, h_w, h_q, h_meta, h_topk, h_o, side):
+    def step_host(self, h_q_idx, h_w, h_q, h_meta, h_topk, h_o, side, h_new_kv=None, h_new_k=None):
         """One step from and to pinned host buffers (same shapes as the device
-        tensors): the indexer inputs and the metadata are copied on the
-        current stream, the attention queries (the largest input, needed only
-        by the attention) on the stream ``side`` while the indexer runs; the
-        token selections of the first full slot and every layer's output are
-        read back at the end. Can be captured in a CUDA graph."""
+        tensors): the indexer inputs, the metadata and the new tokens' rows
+        are copied on the current stream, the attention queries (the largest
+        input, needed only by the attention) on the stream ``side`` while the
+        indexer runs; the token selections of the first full slot and every
+        layer's output are read back at the end. Can be captured in a CUDA
+        graph."""
         cur = torch.cuda.current_stream(self.dev)
         side.wait_stream(cur)  # the previous step has finished reading q
         with torch.cuda.stream(side):
@@ -124,8 +145,13 @@ class LayerRunner:
         self.w.copy_(h_w, non_blocking=True)
         for d, h in zip(self.meta, h_meta):
             d.copy_(h, non_blocking=True)
+        for d, h in zip(self.new_kv, h_new_kv or []):
+            d.copy_(h, non_blocking=True)
+        for d, h in zip(self.new_k, h_new_k or []):
+            d.copy_(h, non_blocking=True)
         joined = False
         for layer in range(len(self.types)):
+            self.write_back(layer)
             if self.full_slot[layer] >= 0:
                 slot = self.full_slot[layer]
                 self.index(slot)
