@@ -15,6 +15,8 @@ namespace dsa {
 
 constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kTopkThreadsShort = 128;  // threads per row when every row has at most kTopkShortCap keys
+constexpr int kTopkShortCap = 8192;
 constexpr int kTopkSmemCap = 32768;  // row elements staged in shared memory
 constexpr int kTopkSmemMax = (kTopkWarps + 1) * 256 * 4 + kTopkSmemCap * 4;
 
@@ -25,8 +27,10 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+template <int TPB>
 __device__ __forceinline__ int block_scan_warps(int v, int* s_tmp, int* total) {
   // exclusive scan of one value per warp (lane 0 holds it) across the block
+  constexpr int kTopkWarps = TPB / 32;
   const int w = warp_id(), lane = lane_id();
   if (lane == 0) s_tmp[w] = v;
   __syncthreads();
@@ -59,14 +63,16 @@ __device__ __forceinline__ void hist_add(uint32_t* wh, uint32_t key, bool valid,
 
 // Pick the digit holding the rank-`remaining` key from the 256-bin histogram
 // (summed over warps) and update prefix / mask / remaining. Block-wide.
+template <int TPB>
 __device__ __forceinline__ void pick_digit(uint32_t* hist, int shift, uint32_t& prefix, uint32_t& mask,
                                            int& remaining, int* s_sel) {
+  constexpr int kTopkWarps = TPB / 32;
   const int tid = threadIdx.x, w = warp_id(), lane = lane_id();
-  if (tid < 256) {
+  for (int b = tid; b < 256; b += TPB) {
     uint32_t c = 0;
 #pragma unroll
-    for (int j = 0; j < kTopkWarps; ++j) c += hist[j * 256 + tid];
-    hist[kTopkWarps * 256 + tid] = c;
+    for (int j = 0; j < kTopkWarps; ++j) c += hist[j * 256 + b];
+    hist[kTopkWarps * 256 + b] = c;
   }
   __syncthreads();
   if (w == 0) {
@@ -107,10 +113,11 @@ __device__ __forceinline__ void pick_digit(uint32_t* hist, int shift, uint32_t& 
 // segment; two block scans give each warp its output offset.
 // With s_idx, entry i of the staged keys stands for row position s_idx[i]
 // (a compacted candidate list kept in ascending position order).
-template <bool kStaged>
+template <bool kStaged, int TPB>
 __device__ void emit_ordered(const float* __restrict__ g, const uint32_t* __restrict__ s_row, int n,
                              uint32_t kstar, int need_eq, int32_t* __restrict__ out_idx, float* __restrict__ out_val,
                              int* s_tmp, const int* __restrict__ s_idx = nullptr) {
+  constexpr int kTopkWarps = TPB / 32;
   const int w = warp_id(), lane = lane_id();
   auto key_at = [&](int i) -> uint32_t { return kStaged ? s_row[i] : ordered_key(__ldg(g + i)); };
   const int seg = ((n + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
@@ -124,9 +131,9 @@ __device__ void emit_ordered(const float* __restrict__ g, const uint32_t* __rest
     eq += __popc(__ballot_sync(0xffffffffu, in && key == kstar));
   }
   int tot;
-  const int eq_base = block_scan_warps(eq, s_tmp, &tot);
+  const int eq_base = block_scan_warps<TPB>(eq, s_tmp, &tot);
   const int take_eq = max(0, min(need_eq - eq_base, eq));
-  const int out_base = block_scan_warps(gt + take_eq, s_tmp, &tot);
+  const int out_base = block_scan_warps<TPB>(gt + take_eq, s_tmp, &tot);
   const uint32_t lt = (1u << lane) - 1u;
   int eq_run = eq_base, sel_run = out_base;
   for (int i = seg0 + lane; i < seg_end; i += 32) {
@@ -209,7 +216,7 @@ __device__ void select_row_global(const float* __restrict__ g, int n, int k, int
       hist_add(wh, in ? ordered_key(__ldg(g + i)) : 0u, in, prefix, mask, shift);
     }
     __syncthreads();
-    pick_digit(hist, shift, prefix, mask, remaining, s_sel);
+    pick_digit<kTopkThreads>(hist, shift, prefix, mask, remaining, s_sel);
   }
   const uint32_t kstar = prefix;
   const int need_eq = remaining;
@@ -261,7 +268,7 @@ __device__ void select_row_global(const float* __restrict__ g, int n, int k, int
   if (neq > list_cap || k > list_cap) {
     // too many winners or ties to collect (the lists stopped at list_cap
     // entries): ordered emission straight from global memory
-    emit_ordered<false>(g, nullptr, n, kstar, need_eq, out_idx, out_val, s_tmp);
+    emit_ordered<false, kTopkThreads>(g, nullptr, n, kstar, need_eq, out_idx, out_val, s_tmp);
     return;
   }
   // lowest-index need_eq ties: sort the tie list, then the k winners
@@ -452,45 +459,52 @@ __device__ bool select_row_two_pass(const float* __restrict__ g, int n, int k, i
     uint32_t* wh = hist + w * 256;
     for (int i = tid; i < mround; i += kTopkThreads) hist_add(wh, i < m ? ckey[i] : 0u, i < m, prefix, mask, shift);
     __syncthreads();
-    pick_digit(hist, shift, prefix, mask, remaining, s_sel);
+    pick_digit<kTopkThreads>(hist, shift, prefix, mask, remaining, s_sel);
   }
-  emit_ordered<true>(g, ckey, m, prefix, remaining, out_idx, out_val, s_tmp, cidx);
+  emit_ordered<true, kTopkThreads>(g, ckey, m, prefix, remaining, out_idx, out_val, s_tmp, cidx);
   return true;
 }
 
 // Row staged in shared memory as ordered keys; the histograms of the first
 // pass (top digit) were counted while staging.
+template <int TPB>
 __device__ void select_row_staged(const float* __restrict__ g, const uint32_t* __restrict__ s_row, int n, int k,
                                   int32_t* __restrict__ out_idx, float* __restrict__ out_val, uint32_t* hist,
                                   int* s_tmp) {
+  constexpr int W = TPB / 32;
   const int tid = threadIdx.x, w = warp_id();
   uint32_t prefix = 0, mask = 0;
   int remaining = k;
   __shared__ int s_sel[2];
-  const int nround = (n + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
-  pick_digit(hist, 24, prefix, mask, remaining, s_sel);
+  const int nround = (n + TPB - 1) / TPB * TPB;
+  pick_digit<TPB>(hist, 24, prefix, mask, remaining, s_sel);
   for (int pass = 1; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-    for (int i = tid; i < kTopkWarps * 256; i += kTopkThreads) hist[i] = 0;
+    for (int i = tid; i < W * 256; i += TPB) hist[i] = 0;
     __syncthreads();
     uint32_t* wh = hist + w * 256;
-    for (int i = tid; i < nround; i += kTopkThreads) hist_add(wh, i < n ? s_row[i] : 0u, i < n, prefix, mask, shift);
+    for (int i = tid; i < nround; i += TPB) hist_add(wh, i < n ? s_row[i] : 0u, i < n, prefix, mask, shift);
     __syncthreads();
-    pick_digit(hist, shift, prefix, mask, remaining, s_sel);
+    pick_digit<TPB>(hist, shift, prefix, mask, remaining, s_sel);
   }
-  emit_ordered<true>(g, s_row, n, prefix, remaining, out_idx, out_val, s_tmp);
+  emit_ordered<true, TPB>(g, s_row, n, prefix, remaining, out_idx, out_val, s_tmp);
 }
 
-__global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const float* __restrict__ scores, long long ld,
-                                                                 const int* __restrict__ nvis, int div, int k,
-                                                                 int32_t* __restrict__ out_idx,
-                                                                 float* __restrict__ out_val, int cap) {
+// TPB threads per row: kTopkThreads (rows of any length) or kTopkThreadsShort
+// (launches whose rows all fit the staging area of kTopkShortCap keys: more
+// rows resident per SM and cheaper block barriers)
+template <int TPB>
+__global__ void __launch_bounds__(TPB) topk_rows_kernel(const float* __restrict__ scores, long long ld,
+                                                        const int* __restrict__ nvis, int div, int k,
+                                                        int32_t* __restrict__ out_idx, float* __restrict__ out_val,
+                                                        int cap) {
+  constexpr int W = TPB / 32;
   griddep_launch_dependents();
   griddep_wait();
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int s_tmp[72];
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem);  // (warps + 1) * 256
-  uint32_t* s_row = hist + (kTopkWarps + 1) * 256;      // cap keys
+  uint32_t* s_row = hist + (W + 1) * 256;               // cap keys
   const int row = blockIdx.x;
   int n = nvis[row];
   if (div > 1) n = (n + div - 1) / div;
@@ -507,19 +521,19 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const float* __
   if (n <= cap) {
     // stage with many independent loads in flight, counting the top digit of
     // every key on the way (the first radix pass)
-    for (int i = threadIdx.x; i < kTopkWarps * 256; i += kTopkThreads) hist[i] = 0;
+    for (int i = threadIdx.x; i < W * 256; i += TPB) hist[i] = 0;
     __syncthreads();
     uint32_t* wh = hist + warp_id() * 256;
-    for (int b0 = 0; b0 < n; b0 += kTopkThreads * 8) {
+    for (int b0 = 0; b0 < n; b0 += TPB * 8) {
       float v[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int i = b0 + u * kTopkThreads + threadIdx.x;
+        const int i = b0 + u * TPB + threadIdx.x;
         v[u] = i < n ? __ldg(g + i) : 0.f;
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int i = b0 + u * kTopkThreads + threadIdx.x;
+        const int i = b0 + u * TPB + threadIdx.x;
         if (i < n) {
           const uint32_t key = ordered_key(v[u]);
           s_row[i] = key;
@@ -528,11 +542,12 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const float* __
       }
     }
     __syncthreads();
-    select_row_staged(g, s_row, n, k, oi, ov, hist, s_tmp);
-  } else {
+    select_row_staged<TPB>(g, s_row, n, k, oi, ov, hist, s_tmp);
+  } else if constexpr (TPB == kTopkThreads) {
     if (cap < kTopkSmemCap || !select_row_two_pass(g, n, k, oi, ov, hist, s_row, s_tmp))
       select_row_global(g, n, k, oi, ov, hist, s_tmp, reinterpret_cast<int*>(s_row), cap / 2);
   }
+  // (the short-row instantiation is only launched when every row fits cap)
 }
 
 int run_topk(cudaStream_t stream, const float* scores, long long ld, const int* nvis, int T, int div, int k,
@@ -544,10 +559,22 @@ int run_topk(cudaStream_t stream, const float* scores, long long ld, const int* 
   // rows longer than the staging capacity use the staging area as two
   // winner lists of cap/2 entries each
   const int cap = max_len > kTopkSmemCap ? kTopkSmemCap : max(0, max_len);
+  // short blocks pay off when their extra rows per SM are there to fill it
+  // (many rows) or the rows are short; a few long rows keep the wide block
+  // (measured: 32 rows of 4-8 K keys took 61 us with short blocks, 41 us wide)
+  if (max_len <= kTopkShortCap && (T >= 2 * sm_count() || max_len <= 2048)) {
+    constexpr int W = kTopkThreadsShort / 32;
+    const size_t smem = (size_t)(W + 1) * 256 * 4 + (size_t)cap * 4;
+    set_smem_attr_once(reinterpret_cast<const void*>(topk_rows_kernel<kTopkThreadsShort>),
+                       (W + 1) * 256 * 4 + kTopkShortCap * 4);
+    DSA_LAUNCH_PDL(topk_rows_kernel<kTopkThreadsShort>, dim3(T), dim3(kTopkThreadsShort), smem, stream, scores, ld,
+                   nvis, div, k, out_idx, out_val, cap);
+    return DSA_OK;
+  }
   const size_t smem = (size_t)(kTopkWarps + 1) * 256 * 4 + (size_t)cap * 4;
-  set_smem_attr_once(reinterpret_cast<const void*>(topk_rows_kernel), (int)(kTopkSmemMax));
-  DSA_LAUNCH_PDL(topk_rows_kernel, dim3(T), dim3(kTopkThreads), smem, stream, scores, ld, nvis, div, k, out_idx,
-                 out_val, cap);
+  set_smem_attr_once(reinterpret_cast<const void*>(topk_rows_kernel<kTopkThreads>), (int)(kTopkSmemMax));
+  DSA_LAUNCH_PDL(topk_rows_kernel<kTopkThreads>, dim3(T), dim3(kTopkThreads), smem, stream, scores, ld, nvis, div,
+                 k, out_idx, out_val, cap);
   return DSA_OK;
 }
 
