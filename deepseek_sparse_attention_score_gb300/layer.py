@@ -128,19 +128,32 @@ class LayerRunner:
         for layer in range(len(self.types)):
             self.layer_step(layer)
 
-    def step_host(self, h_q_idx, h_w, h_q, h_meta, h_topk, h_o, side, h_new_kv=None, h_new_k=None):
+    def step_host(self, h_q_idx, h_w, h_q, h_meta, h_topk, h_o, side, h_new_kv=None, h_new_k=None, out_side=None):
         """One step from and to pinned host buffers (same shapes as the device
-        tensors): the indexer inputs, the metadata and the new tokens' rows
-        are copied on the current stream, the attention queries (the largest
-        input, needed only by the attention) on the stream ``side`` while the
-        indexer runs; the token selections of the first full slot and every
-        layer's output are read back at the end. Can be captured in a CUDA
-        graph."""
+        tensors). The indexer inputs, the metadata and the new tokens' rows
+        are copied on the current stream; each layer's attention queries (the
+        largest inputs, needed only by that layer's attention) on the stream
+        ``side``, in layer order, while the earlier layers compute; each
+        layer's output is read back on the stream ``out_side`` (one of the
+        runner's own if None) as soon as that layer's attention has written it,
+        and the token selections of the first full slot once they exist. The
+        current stream joins both side streams before it returns, so the step
+        ends when every copy has landed. Can be captured in a CUDA graph."""
         cur = torch.cuda.current_stream(self.dev)
-        side.wait_stream(cur)  # the previous step has finished reading q
+        if out_side is None:
+            if getattr(self, "_out_side", None) is None:
+                self._out_side = torch.cuda.Stream(self.dev)
+            out_side = self._out_side
+        # the previous step's kernels have finished reading q (its read-backs
+        # were joined into the current stream when it returned)
+        side.wait_stream(cur)
+        q_ready = []
         with torch.cuda.stream(side):
             for d, h in zip(self.q, h_q):
                 d.copy_(h, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(side)
+                q_ready.append(ev)
         self.q_idx.copy_(h_q_idx, non_blocking=True)
         self.w.copy_(h_w, non_blocking=True)
         for d, h in zip(self.meta, h_meta):
@@ -149,7 +162,7 @@ class LayerRunner:
             d.copy_(h, non_blocking=True)
         for d, h in zip(self.new_k, h_new_k or []):
             d.copy_(h, non_blocking=True)
-        joined = False
+        topk_read = False
         for layer in range(len(self.types)):
             self.write_back(layer)
             if self.full_slot[layer] >= 0:
@@ -157,10 +170,15 @@ class LayerRunner:
                 self.index(slot)
                 if self.prefill:
                     self.union(slot)
-            if not joined:
-                cur.wait_stream(side)
-                joined = True
+                if not topk_read:
+                    out_side.wait_stream(cur)
+                    with torch.cuda.stream(out_side):
+                        h_topk.copy_(self.topk[0], non_blocking=True)
+                    topk_read = True
+            cur.wait_event(q_ready[layer])
             self.attend(layer)
-        h_topk.copy_(self.topk[0], non_blocking=True)
-        for h, d in zip(h_o, self.o):
-            h.copy_(d, non_blocking=True)
+            out_side.wait_stream(cur)
+            with torch.cuda.stream(out_side):
+                h_o[layer].copy_(self.o[layer], non_blocking=True)
+        cur.wait_stream(side)
+        cur.wait_stream(out_side)
