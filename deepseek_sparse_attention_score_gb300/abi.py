@@ -41,6 +41,7 @@ EXPORTS = (
     "dsa_sparse_mla_decode_workspace_size",
     "dsa_sparse_mla_decode",
     "dsa_sparse_mla_prefill_qblock",
+    "dsa_sparse_mla_prefill_qblock_range",
     "dsa_paged_write_back",
     "dsa_dense_mla",
     "dsa_selftest_wait_timeout",
@@ -90,6 +91,8 @@ def lib() -> ctypes.CDLL:
                                         _F, _P, _P, _P, _Z, _P]
     L.dsa_sparse_mla_prefill_qblock.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                                 _I, _I, _I, _I, _F, _P, _P, _P]
+    L.dsa_sparse_mla_prefill_qblock_range.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                                      _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _P]
     L.dsa_sparse_mla_decode_noalloc.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                                 _I, _I, _F, _P, _P, _P]
     L.dsa_paged_write_back.argtypes = [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]
@@ -289,9 +292,12 @@ def dsa_sparse_mla_decode(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, 
 
 
 def dsa_sparse_mla_prefill_qblock(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_indices, units, member, counts, *,
-                                  QB, sm_scale, o=None, lse=None, want_lse=False, dev_status=None, Dv=512):
+                                  QB, sm_scale, o=None, lse=None, want_lse=False, dev_status=None, Dv=512,
+                                  t_range=None):
     """Query-block sparse-MLA prefill over the union tables of
-    ``dsa_build_block_union`` (same QB and u_max)."""
+    ``dsa_build_block_union`` (same QB and u_max). ``t_range=(b, e)``
+    computes only the output rows of tokens b .. e-1
+    (``dsa_sparse_mla_prefill_qblock_range``)."""
     dev = q.device
     _need(q, "q", torch.bfloat16, dev, 3)
     _need(kv, "kv", torch.bfloat16, dev, 3)
@@ -306,11 +312,18 @@ def dsa_sparse_mla_prefill_qblock(q, kv, seq_lens, cu_q_lens, cu_kv_lens, page_i
         o = torch.empty((T, H, Dv), dtype=torch.bfloat16, device=dev)
     if want_lse and lse is None:
         lse = torch.empty((T, H), dtype=torch.float32, device=dev)
-    rc = lib().dsa_sparse_mla_prefill_qblock(_stream(dev), _ptr(q), _ptr(kv), row_stride, _ptr(seq_lens),
-                                             _ptr(cu_q_lens), _ptr(cu_kv_lens), _ptr(page_indices), _ptr(units),
-                                             _ptr(member), _ptr(counts), QB, u_max, T, S, P, PTW, ps, H, Dk, Dv,
-                                             float(sm_scale), _ptr(o), _ptr(lse), _ptr(dev_status))
-    _check("dsa_sparse_mla_prefill_qblock", rc)
+    if t_range is None:
+        rc = lib().dsa_sparse_mla_prefill_qblock(_stream(dev), _ptr(q), _ptr(kv), row_stride, _ptr(seq_lens),
+                                                 _ptr(cu_q_lens), _ptr(cu_kv_lens), _ptr(page_indices), _ptr(units),
+                                                 _ptr(member), _ptr(counts), QB, u_max, T, S, P, PTW, ps, H, Dk, Dv,
+                                                 float(sm_scale), _ptr(o), _ptr(lse), _ptr(dev_status))
+        _check("dsa_sparse_mla_prefill_qblock", rc)
+    else:
+        rc = lib().dsa_sparse_mla_prefill_qblock_range(
+            _stream(dev), _ptr(q), _ptr(kv), row_stride, _ptr(seq_lens), _ptr(cu_q_lens), _ptr(cu_kv_lens),
+            _ptr(page_indices), _ptr(units), _ptr(member), _ptr(counts), QB, u_max, T, S, P, PTW, ps, H, Dk, Dv,
+            float(sm_scale), int(t_range[0]), int(t_range[1]), _ptr(o), _ptr(lse), _ptr(dev_status))
+        _check("dsa_sparse_mla_prefill_qblock_range", rc)
     return (o, lse) if lse is not None else o
 
 

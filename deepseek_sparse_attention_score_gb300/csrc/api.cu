@@ -428,21 +428,21 @@ int dsa_sparse_mla_decode_noalloc(dsa_stream_t stream, const uint16_t* q, const 
   return run_attend_static_scratch(static_cast<cudaStream_t>(stream), prm);
 }
 
-int dsa_sparse_mla_prefill_qblock(dsa_stream_t stream, const uint16_t* q, const uint16_t* kv, int row_stride,
-                                  const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
-                                  const int32_t* page_indices, const int32_t* units, const uint32_t* member,
-                                  const int32_t* counts, int QB, int u_max, int T, int S, int P, int PTW, int ps,
-                                  int H, int Dk, int Dv, float sm_scale, uint16_t* o, float* lse,
-                                  int32_t* dev_status) {
-  NvtxRange nvtx_range("dsa_sparse_mla_prefill_qblock");
+static int qblock_common(cudaStream_t stream, const uint16_t* q, const uint16_t* kv, int row_stride,
+                         const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
+                         const int32_t* page_indices, const int32_t* units, const uint32_t* member,
+                         const int32_t* counts, int QB, int u_max, int T, int S, int P, int PTW, int ps, int H, int Dk,
+                         int Dv, float sm_scale, int t_begin, int t_end, uint16_t* o, float* lse,
+                         int32_t* dev_status) {
   int rc = check_meta(seq_lens, cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps);
   if (rc) return rc;
   rc = attend_check(q, kv, row_stride, T, H, Dk, Dv, o);
   if (rc) return rc;
   if (QB < 32 || QB % 32 != 0 || u_max < 1) return DSA_ERR_INVALID_ARGUMENT;
+  if (t_begin < 0 || t_end < t_begin || t_end > T) return DSA_ERR_INVALID_ARGUMENT;
   if (T > 0 && (!units || !member || !counts)) return DSA_ERR_INVALID_ARGUMENT;
   if (!std::isfinite(sm_scale)) return DSA_ERR_INVALID_ARGUMENT;
-  if (T == 0 || H == 0) return DSA_OK;
+  if (t_end == t_begin || H == 0) return DSA_OK;
   AttendParams prm{};
   prm.q = q;
   prm.kv = kv;
@@ -466,10 +466,37 @@ int dsa_sparse_mla_prefill_qblock(dsa_stream_t stream, const uint16_t* q, const 
   prm.u_max = u_max;
   prm.K = 1;
   prm.nsplit = 1;
+  prm.t0 = t_begin;
+  prm.tn = t_end - t_begin;
   prm.o = o;
   prm.lse = lse;
   prm.dev_status = dev_status;
-  return run_attend(static_cast<cudaStream_t>(stream), prm, nullptr, 0);
+  return run_attend(stream, prm, nullptr, 0);
+}
+
+int dsa_sparse_mla_prefill_qblock(dsa_stream_t stream, const uint16_t* q, const uint16_t* kv, int row_stride,
+                                  const int32_t* seq_lens, const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
+                                  const int32_t* page_indices, const int32_t* units, const uint32_t* member,
+                                  const int32_t* counts, int QB, int u_max, int T, int S, int P, int PTW, int ps,
+                                  int H, int Dk, int Dv, float sm_scale, uint16_t* o, float* lse,
+                                  int32_t* dev_status) {
+  NvtxRange nvtx_range("dsa_sparse_mla_prefill_qblock");
+  return qblock_common(static_cast<cudaStream_t>(stream), q, kv, row_stride, seq_lens, cu_q_lens, cu_kv_lens,
+                       page_indices, units, member, counts, QB, u_max, T, S, P, PTW, ps, H, Dk, Dv, sm_scale, 0,
+                       T < 0 ? 0 : T, o, lse, dev_status);
+}
+
+int dsa_sparse_mla_prefill_qblock_range(dsa_stream_t stream, const uint16_t* q, const uint16_t* kv, int row_stride,
+                                        const int32_t* seq_lens, const int32_t* cu_q_lens,
+                                        const int32_t* cu_kv_lens, const int32_t* page_indices,
+                                        const int32_t* units, const uint32_t* member, const int32_t* counts, int QB,
+                                        int u_max, int T, int S, int P, int PTW, int ps, int H, int Dk, int Dv,
+                                        float sm_scale, int t_begin, int t_end, uint16_t* o, float* lse,
+                                        int32_t* dev_status) {
+  NvtxRange nvtx_range("dsa_sparse_mla_prefill_qblock_range");
+  return qblock_common(static_cast<cudaStream_t>(stream), q, kv, row_stride, seq_lens, cu_q_lens, cu_kv_lens,
+                       page_indices, units, member, counts, QB, u_max, T, S, P, PTW, ps, H, Dk, Dv, sm_scale,
+                       t_begin, t_end, o, lse, dev_status);
 }
 
 }  // extern "C"

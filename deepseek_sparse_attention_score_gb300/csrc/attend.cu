@@ -374,7 +374,7 @@ __global__ void __launch_bounds__((6 + kCopyW) * 32, 1)
   constexpr int n_copy_warps = kCopyW;
   constexpr int n_copy_threads = n_copy_warps * 32;
   const int half = blockIdx.x & 1, hg = blockIdx.x >> 1;
-  const int t = blockIdx.y, split = blockIdx.z;
+  const int t = prm.t0 + (int)blockIdx.y, split = blockIdx.z;
   const int h0 = hg * 128;
   uint8_t* qs_s = smem + OFF_QS;
   uint8_t* kst_s = smem + OFF_KST;
@@ -1001,7 +1001,7 @@ int run_attend(cudaStream_t stream, AttendParams prm, void* ws, size_t ws_bytes)
   if (!encode_bf16_2d(&kvmap, prm.kv, (uint64_t)prm.P * prm.ps, (uint64_t)prm.row_stride, 32, kDk))
     return DSA_ERR_CUDA;
   if (!encode_bf16_2d(&qmap, prm.q, (uint64_t)prm.T * prm.H, kDk, 128, kDk)) return DSA_ERR_CUDA;
-  dim3 grid(cols, prm.T, prm.nsplit);
+  dim3 grid(cols, prm.tn > 0 ? prm.tn : prm.T, prm.nsplit);
   void (*kern)(AttendParams, CUtensorMap, CUtensorMap);
   int threads;
   if (prm.soft_cap_on) {  // dense mode only: page runs

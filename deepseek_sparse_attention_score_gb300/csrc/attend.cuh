@@ -30,6 +30,8 @@ struct AttendParams {
   float inv_cap_scale;  // sm_scale / cap
   float cap_log2;       // cap * log2(e)
   int nsplit;
+  int t0;  // first query token of the launch (grid.y walks tokens t0 .. t0 + tn - 1)
+  int tn;  // tokens in the launch; 0 means all T
   uint16_t* o;      // bf16 [T, H, 512]
   float* lse;       // [T, H] or null
   float* o_part;    // [nsplit, T, H, 512] (set by run_attend)

@@ -99,12 +99,15 @@ class LayerRunner:
                                   cu_kv_lens=self.meta[2], ps=self.ps, PTW=self.PTW, units=self.units[slot],
                                   member=self.member[slot], counts=self.counts[slot], dev_status=self.status)
 
-    def attend(self, layer):
+    def attend(self, layer, t_range=None):
+        """The layer's attention; ``t_range=(b, e)`` (prefill batches) writes
+        only the output rows of tokens b .. e-1."""
         slot = self.src_slot[layer]
         if self.prefill:
             abi.dsa_sparse_mla_prefill_qblock(self.q[layer], self.kv[layer], *self.meta, self.units[slot],
                                               self.member[slot], self.counts[slot], QB=self.QB,
-                                              sm_scale=self.wl.sm_scale, o=self.o[layer], dev_status=self.status)
+                                              sm_scale=self.wl.sm_scale, o=self.o[layer], dev_status=self.status,
+                                              t_range=t_range)
         elif self.page_budget is not None:
             abi.dsa_sparse_mla_decode(self.q[layer], self.kv[layer], *self.meta, self.topk_pages[slot],
                                       unit=self.ps, sm_scale=self.wl.sm_scale, o=self.o[layer], ws=self.ws_att,
@@ -128,7 +131,8 @@ class LayerRunner:
         for layer in range(len(self.types)):
             self.layer_step(layer)
 
-    def step_host(self, h_q_idx, h_w, h_q, h_meta, h_topk, h_o, side, h_new_kv=None, h_new_k=None, out_side=None):
+    def step_host(self, h_q_idx, h_w, h_q, h_meta, h_topk, h_o, side, h_new_kv=None, h_new_k=None, out_side=None,
+                  last_chunks=4):
         """One step from and to pinned host buffers (same shapes as the device
         tensors). The indexer inputs, the metadata and the new tokens' rows
         are copied on the current stream; each layer's attention queries (the
@@ -136,9 +140,12 @@ class LayerRunner:
         ``side``, in layer order, while the earlier layers compute; each
         layer's output is read back on the stream ``out_side`` (one of the
         runner's own if None) as soon as that layer's attention has written it,
-        and the token selections of the first full slot once they exist. The
-        current stream joins both side streams before it returns, so the step
-        ends when every copy has landed. Can be captured in a CUDA graph."""
+        and the token selections of the first full slot once they exist. On a
+        prefill batch the last layer's attention runs in ``last_chunks`` token
+        ranges, each read back as soon as it is written, so little of the
+        final read-back is left after the last kernel. The current stream
+        joins both side streams before it returns, so the step ends when every
+        copy has landed. Can be captured in a CUDA graph."""
         cur = torch.cuda.current_stream(self.dev)
         if out_side is None:
             if getattr(self, "_out_side", None) is None:
@@ -176,9 +183,16 @@ class LayerRunner:
                         h_topk.copy_(self.topk[0], non_blocking=True)
                     topk_read = True
             cur.wait_event(q_ready[layer])
-            self.attend(layer)
-            out_side.wait_stream(cur)
-            with torch.cuda.stream(out_side):
-                h_o[layer].copy_(self.o[layer], non_blocking=True)
+            last = layer == len(self.types) - 1
+            nch = max(1, min(last_chunks, self.T // self.QB)) if (self.prefill and last) else 1
+            bounds = [0, self.T]
+            if nch > 1:  # token ranges on query-block boundaries
+                nqb = -(-self.T // self.QB)
+                bounds = [min(self.T, (nqb * c // nch) * self.QB) for c in range(nch)] + [self.T]
+            for b, e in zip(bounds[:-1], bounds[1:]):
+                self.attend(layer, (b, e) if nch > 1 else None)
+                out_side.wait_stream(cur)
+                with torch.cuda.stream(out_side):
+                    h_o[layer][b:e].copy_(self.o[layer][b:e], non_blocking=True)
         cur.wait_stream(side)
         cur.wait_stream(out_side)

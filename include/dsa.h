@@ -236,6 +236,27 @@ DSA_API int dsa_sparse_mla_prefill_qblock(dsa_stream_t stream, const uint16_t* q
                                   int32_t* dev_status);
 
 /* ------------------------------------------------------------------------
+ * Query-block sparse-MLA prefill for a contiguous range of query tokens.
+ * The pages have no counterpart of this entry point: it computes the rows
+ * t_begin <= t < t_end of dsa_sparse_mla_prefill_qblock's output, with the
+ * same arithmetic (bit for bit), and writes no other row. A caller that runs
+ * one layer's attention in a few token ranges can start copying the finished
+ * rows off the GPU while the later ranges compute.
+ *   t_begin, t_end  0 <= t_begin <= t_end <= T (t_begin == t_end: nothing)
+ *   every other argument as dsa_sparse_mla_prefill_qblock (q, o and lse keep
+ *   their full [T, ...] extent; token t stays row t)
+ * Errors: as dsa_sparse_mla_prefill_qblock; DSA_ERR_INVALID_ARGUMENT for a
+ * range outside [0, T].
+ * ------------------------------------------------------------------------ */
+DSA_API int dsa_sparse_mla_prefill_qblock_range(dsa_stream_t stream, const uint16_t* q, const uint16_t* kv,
+                                                int row_stride, const int32_t* seq_lens, const int32_t* cu_q_lens,
+                                                const int32_t* cu_kv_lens, const int32_t* page_indices,
+                                                const int32_t* units, const uint32_t* member, const int32_t* counts,
+                                                int QB, int u_max, int T, int S, int P, int PTW, int ps, int H,
+                                                int Dk, int Dv, float sm_scale, int t_begin, int t_end, uint16_t* o,
+                                                float* lse, int32_t* dev_status);
+
+/* ------------------------------------------------------------------------
  * Approximate token top-k (the trade the pages make with approx_max_k on
  * their fast path; ref.py, streamindex_topk_ref is the exact definition).
  * Scores as dsa_indexer_topk. A row of n visible scores is folded into

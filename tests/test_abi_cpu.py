@@ -276,3 +276,19 @@ def _qblock_args(**kw):
 ])
 def test_prefill_qblock_host_checks(dsa, kw, code):
     assert dsa.lib().dsa_sparse_mla_prefill_qblock(*_qblock_args(**kw)) == code
+
+
+def _qblock_range_args(t_begin, t_end, **kw):
+    a = _qblock_args(**kw)
+    # the range goes between sm_scale and o
+    return a[:22] + [t_begin, t_end] + a[22:]
+
+
+@pytest.mark.parametrize("tb,te,code", [
+    (-1, 8, INVALID),
+    (8, 4, INVALID),
+    (0, 65, INVALID),
+    (5, 5, OK),      # an empty range enqueues nothing
+])
+def test_prefill_qblock_range_host_checks(dsa, tb, te, code):
+    assert dsa.lib().dsa_sparse_mla_prefill_qblock_range(*_qblock_range_args(tb, te)) == code
