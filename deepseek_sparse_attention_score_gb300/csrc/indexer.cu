@@ -526,8 +526,16 @@ int run_indexer(cudaStream_t stream, const IndexerMeta& m, const uint16_t* q, co
   CUtensorMap qmap8;
   if (!encode_bf16_2d(&qmap8, q, (uint64_t)m.T * 32, 128, 256, 128)) return DSA_ERR_CUDA;
 
-  DSA_LAUNCH_PDL(indexer_plan_kernel, dim3(1), dim3(1024), 0, stream, m, pl, kChunkDecode, kChunkPrefill);
   const int sms = sm_count();
+  // keys per one-token work item: 512, doubled while the decode keys (at most
+  // T x max_kv) still give every SM four items or more, up to 64 pages
+  // (measured: long-context decode 0.55 -> 0.44 ms with 4096-key items; fewer
+  // item boundaries, where a persistent CTA waits on the next item's
+  // metadata and query, in the key stream)
+  int ch1 = kChunkDecode;
+  const long long decode_keys = (long long)m.T * m.max_kv;
+  while (ch1 < kChunkDecodeMax && 2 * ch1 <= 64 * m.ps && decode_keys / (2LL * ch1) >= 4LL * sms) ch1 *= 2;
+  DSA_LAUNCH_PDL(indexer_plan_kernel, dim3(1), dim3(1024), 0, stream, m, pl, ch1, kChunkPrefill);
   {
     using C = IdxCfg<1>;
     set_smem_attr_once(reinterpret_cast<const void*>(indexer_score_kernel<1>), C::SMEM);

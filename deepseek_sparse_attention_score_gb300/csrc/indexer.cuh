@@ -6,8 +6,9 @@
 
 namespace dsa {
 
-constexpr int kChunkDecode = 512;    // keys per work item of one-token tiles
-constexpr int kChunkPrefill = 2048;  // keys per work item of 8-token tiles
+constexpr int kChunkDecode = 512;      // keys per work item of one-token tiles (at least)
+constexpr int kChunkDecodeMax = 4096;  // ... and at most
+constexpr int kChunkPrefill = 2048;    // keys per work item of 8-token tiles
 
 struct IndexerMeta {
   const float* w;
