@@ -178,10 +178,12 @@ def committed_traffic(kernel_key, workload):
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             d = json.load(f)[f"{kernel_key}@{workload}"]
-        src = os.path.join(ROOT, d["source"])
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        return d["bytes_per_launch"] if h == d["source_sha256_16"] else None
-    except Exception:
+        for src, want in d["sources"].items():
+            with open(os.path.join(ROOT, src), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest()[:16] != want:
+                    return None
+        return d["bytes_per_launch"]
+    except (OSError, KeyError, ValueError):
         return None
 
 

@@ -17,8 +17,7 @@ constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kTopkThreadsShort = 128;  // threads per row when every row has at most kTopkShortCap keys
 constexpr int kTopkShortCap = 8192;
-constexpr int kTopkSmemCap = 32768;  // row elements staged in shared memory
-constexpr int kTopkSmemMax = (kTopkWarps + 1) * 256 * 4 + kTopkSmemCap * 4;
+constexpr int kTopkThreadsMany = 256;   // threads per row for many rows of any length
 
 // Order-preserving map fp32 -> uint32 (larger float -> larger key); -0 and +0
 // map to the same key so they tie like equal scores.
@@ -179,9 +178,11 @@ constexpr int kUnroll = 16;  // float4 loads in flight per thread on the global 
 // Row longer than shared memory: radix passes read it from global memory
 // (L2) with many loads in flight; the final pass collects the winners
 // unordered and sorts them.
+template <int TPB>
 __device__ void select_row_global(const float* __restrict__ g, int n, int k, int32_t* __restrict__ out_idx,
                                   float* __restrict__ out_val, uint32_t* hist, int* s_tmp, int* lists,
                                   int list_cap) {
+  constexpr int kTopkThreads = TPB, kTopkWarps = TPB / 32;
   const int tid = threadIdx.x, w = warp_id();
   uint32_t prefix = 0, mask = 0;
   int remaining = k;
@@ -216,7 +217,7 @@ __device__ void select_row_global(const float* __restrict__ g, int n, int k, int
       hist_add(wh, in ? ordered_key(__ldg(g + i)) : 0u, in, prefix, mask, shift);
     }
     __syncthreads();
-    pick_digit<kTopkThreads>(hist, shift, prefix, mask, remaining, s_sel);
+    pick_digit<TPB>(hist, shift, prefix, mask, remaining, s_sel);
   }
   const uint32_t kstar = prefix;
   const int need_eq = remaining;
@@ -268,7 +269,7 @@ __device__ void select_row_global(const float* __restrict__ g, int n, int k, int
   if (neq > list_cap || k > list_cap) {
     // too many winners or ties to collect (the lists stopped at list_cap
     // entries): ordered emission straight from global memory
-    emit_ordered<false, kTopkThreads>(g, nullptr, n, kstar, need_eq, out_idx, out_val, s_tmp);
+    emit_ordered<false, TPB>(g, nullptr, n, kstar, need_eq, out_idx, out_val, s_tmp);
     return;
   }
   // lowest-index need_eq ties: sort the tie list, then the k winners
@@ -305,12 +306,18 @@ __device__ void select_row_global(const float* __restrict__ g, int n, int k, int
 constexpr int kWideBits = 11;
 constexpr int kWideBins = 1 << kWideBits;
 constexpr int kWideShift = 32 - kWideBits;
-constexpr int kCandCap = kTopkSmemCap / 2;  // candidates: keys + positions in the staging area
-static_assert(kTopkWarps * kWideBins <= kTopkSmemCap, "per-warp wide histograms fit the staging area");
-static_assert(kTopkThreads * 4 == kWideBins, "four wide bins per thread");
+// The staging area of a TPB-thread block holds (TPB / 32) * kWideBins keys:
+// exactly the per-warp wide histograms, and then the candidate list (keys and
+// positions) of half as many entries.
+template <int TPB>
+__host__ __device__ constexpr int stage_cap() { return TPB / 32 * kWideBins; }
 
+template <int TPB>
 __device__ bool select_row_two_pass(const float* __restrict__ g, int n, int k, int32_t* __restrict__ out_idx,
                                     float* __restrict__ out_val, uint32_t* hist, uint32_t* area, int* s_tmp) {
+  constexpr int kTopkThreads = TPB, kTopkWarps = TPB / 32;
+  constexpr int kCandCap = stage_cap<TPB>() / 2;
+  constexpr int BPT = kWideBins / TPB;  // wide bins per thread in the scan
   const int tid = threadIdx.x, w = warp_id(), lane = lane_id();
   __shared__ int s_sel[2];
   __shared__ int s_woff[kTopkWarps + 1];
@@ -342,11 +349,11 @@ __device__ bool select_row_two_pass(const float* __restrict__ g, int n, int k, i
   }
   __syncthreads();
   // bin totals, scanned from the top bin down: thread tid owns bins
-  // 2047 - 4*tid .. 2044 - 4*tid
-  uint32_t cnt[4], tot = 0;
+  // 2047 - BPT*tid .. 2048 - BPT*(tid + 1)
+  uint32_t cnt[BPT], tot = 0;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int bin = kWideBins - 1 - (4 * tid + j);
+  for (int j = 0; j < BPT; ++j) {
+    const int bin = kWideBins - 1 - (BPT * tid + j);
     uint32_t c = 0;
 #pragma unroll 4
     for (int ww = 0; ww < kTopkWarps; ++ww) c += area[ww * kWideBins + bin];
@@ -375,9 +382,9 @@ __device__ bool select_row_two_pass(const float* __restrict__ g, int n, int k, i
   __syncthreads();
   uint32_t above = (uint32_t)s_tmp[32 + w] + (x - tot);  // keys in bins above this thread's first bin
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < BPT; ++j) {
     if (above < (uint32_t)k && above + cnt[j] >= (uint32_t)k) {
-      s_sel[0] = kWideBins - 1 - (4 * tid + j);
+      s_sel[0] = kWideBins - 1 - (BPT * tid + j);
       s_sel[1] = (int)(above + cnt[j]);  // candidates: keys in bins >= b*
     }
     above += cnt[j];
@@ -459,9 +466,9 @@ __device__ bool select_row_two_pass(const float* __restrict__ g, int n, int k, i
     uint32_t* wh = hist + w * 256;
     for (int i = tid; i < mround; i += kTopkThreads) hist_add(wh, i < m ? ckey[i] : 0u, i < m, prefix, mask, shift);
     __syncthreads();
-    pick_digit<kTopkThreads>(hist, shift, prefix, mask, remaining, s_sel);
+    pick_digit<TPB>(hist, shift, prefix, mask, remaining, s_sel);
   }
-  emit_ordered<true, kTopkThreads>(g, ckey, m, prefix, remaining, out_idx, out_val, s_tmp, cidx);
+  emit_ordered<true, TPB>(g, ckey, m, prefix, remaining, out_idx, out_val, s_tmp, cidx);
   return true;
 }
 
@@ -490,14 +497,14 @@ __device__ void select_row_staged(const float* __restrict__ g, const uint32_t* _
   emit_ordered<true, TPB>(g, s_row, n, prefix, remaining, out_idx, out_val, s_tmp);
 }
 
-// TPB threads per row: kTopkThreads (rows of any length) or kTopkThreadsShort
-// (launches whose rows all fit the staging area of kTopkShortCap keys: more
-// rows resident per SM and cheaper block barriers)
+// TPB threads per row: kTopkThreads (a few rows of any length: the shortest
+// per-row time), kTopkThreadsMany (many rows, some long: three rows resident
+// per SM instead of one) or kTopkThreadsShort (many rows that all fit a
+// stage of kTopkShortCap keys)
 template <int TPB>
-__global__ void __launch_bounds__(TPB) topk_rows_kernel(const float* __restrict__ scores, long long ld,
-                                                        const int* __restrict__ nvis, int div, int k,
-                                                        int32_t* __restrict__ out_idx, float* __restrict__ out_val,
-                                                        int cap) {
+__global__ void __launch_bounds__(TPB, TPB == kTopkThreadsMany ? 3 : 1)
+    topk_rows_kernel(const float* __restrict__ scores, long long ld, const int* __restrict__ nvis, int div, int k,
+                     int32_t* __restrict__ out_idx, float* __restrict__ out_val, int cap) {
   constexpr int W = TPB / 32;
   griddep_launch_dependents();
   griddep_wait();
@@ -543,9 +550,9 @@ __global__ void __launch_bounds__(TPB) topk_rows_kernel(const float* __restrict_
     }
     __syncthreads();
     select_row_staged<TPB>(g, s_row, n, k, oi, ov, hist, s_tmp);
-  } else if constexpr (TPB == kTopkThreads) {
-    if (cap < kTopkSmemCap || !select_row_two_pass(g, n, k, oi, ov, hist, s_row, s_tmp))
-      select_row_global(g, n, k, oi, ov, hist, s_tmp, reinterpret_cast<int*>(s_row), cap / 2);
+  } else if constexpr (TPB != kTopkThreadsShort) {
+    if (cap < stage_cap<TPB>() || !select_row_two_pass<TPB>(g, n, k, oi, ov, hist, s_row, s_tmp))
+      select_row_global<TPB>(g, n, k, oi, ov, hist, s_tmp, reinterpret_cast<int*>(s_row), cap / 2);
   }
   // (the short-row instantiation is only launched when every row fits cap)
 }
@@ -557,25 +564,27 @@ int run_topk(cudaStream_t stream, const float* scores, long long ld, const int* 
   // start 16-byte aligned
   if ((ld & 3) || (reinterpret_cast<uintptr_t>(scores) & 15)) return DSA_ERR_ALIGNMENT;
   // rows longer than the staging capacity use the staging area as two
-  // winner lists of cap/2 entries each
-  const int cap = max_len > kTopkSmemCap ? kTopkSmemCap : max(0, max_len);
+  // winner lists of cap/2 entries each; the staging capacity of a block size
+  // is its wide-histogram area (stage_cap)
+  auto launch = [&](auto tpb_c) -> int {
+    constexpr int TPB = decltype(tpb_c)::value;
+    constexpr int W = TPB / 32;
+    const int cap = max_len > stage_cap<TPB>() ? stage_cap<TPB>() : max(0, max_len);
+    const size_t smem = (size_t)(W + 1) * 256 * 4 + (size_t)cap * 4;
+    set_smem_attr_once(reinterpret_cast<const void*>(topk_rows_kernel<TPB>),
+                       (W + 1) * 256 * 4 + stage_cap<TPB>() * 4);
+    DSA_LAUNCH_PDL(topk_rows_kernel<TPB>, dim3(T), dim3(TPB), smem, stream, scores, ld, nvis, div, k, out_idx,
+                   out_val, cap);
+    return DSA_OK;
+  };
+  const bool many = T >= 2 * sm_count();
   // short blocks pay off when their extra rows per SM are there to fill it
   // (many rows) or the rows are short; a few long rows keep the wide block
   // (measured: 32 rows of 4-8 K keys took 61 us with short blocks, 41 us wide)
-  if (max_len <= kTopkShortCap && (T >= 2 * sm_count() || max_len <= 2048)) {
-    constexpr int W = kTopkThreadsShort / 32;
-    const size_t smem = (size_t)(W + 1) * 256 * 4 + (size_t)cap * 4;
-    set_smem_attr_once(reinterpret_cast<const void*>(topk_rows_kernel<kTopkThreadsShort>),
-                       (W + 1) * 256 * 4 + kTopkShortCap * 4);
-    DSA_LAUNCH_PDL(topk_rows_kernel<kTopkThreadsShort>, dim3(T), dim3(kTopkThreadsShort), smem, stream, scores, ld,
-                   nvis, div, k, out_idx, out_val, cap);
-    return DSA_OK;
-  }
-  const size_t smem = (size_t)(kTopkWarps + 1) * 256 * 4 + (size_t)cap * 4;
-  set_smem_attr_once(reinterpret_cast<const void*>(topk_rows_kernel<kTopkThreads>), (int)(kTopkSmemMax));
-  DSA_LAUNCH_PDL(topk_rows_kernel<kTopkThreads>, dim3(T), dim3(kTopkThreads), smem, stream, scores, ld, nvis, div,
-                 k, out_idx, out_val, cap);
-  return DSA_OK;
+  if (max_len <= kTopkShortCap && (many || max_len <= 2048))
+    return launch(std::integral_constant<int, kTopkThreadsShort>{});
+  if (many) return launch(std::integral_constant<int, kTopkThreadsMany>{});
+  return launch(std::integral_constant<int, kTopkThreads>{});
 }
 
 }  // namespace dsa

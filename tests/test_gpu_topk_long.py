@@ -77,3 +77,41 @@ def test_long_rows_k_above_the_winner_lists(dsa):
     got = topk.cpu().numpy()
     check_topk_rows(got, ref, k, rows)
     assert np.array_equal(got[2], np.arange(k))  # the all-tie row: the lowest k positions
+
+
+def test_many_long_rows_token_topk(dsa):
+    """More long rows than twice the SM count (the launch shape of a long
+    prefill): random rows, rows of four distinct score values (tie lists
+    longer than the winner lists) and all-zero rows, checked on a sample of
+    rows against the oracle."""
+    dev = torch.device("cuda")
+    n_per = dsa.dsa_device_sm_count() + 8
+    kv_lens = [36000, 33000]
+    wl = DI.random_small(79, [n_per, n_per], kv_lens, H=16, k=2048)
+    rg = wl.rg
+    ps = rg.page_size
+    kc = wl.kcache[0].view(-1, 128)
+    base = int(rg.cu_kv_lens[1]) // ps
+    n1 = kv_lens[1]
+    rows = rg.page_indices[base + np.arange(n1) // ps].astype(np.int64) * ps + np.arange(n1) % ps
+    protos = torch.randn((4, 128), generator=torch.Generator().manual_seed(6)).to(torch.bfloat16)
+    kc[torch.from_numpy(rows)] = protos[torch.from_numpy(np.arange(n1) % 4)]
+    zero_tok = [3, 40, n_per - 1]
+    wl.q_idx[zero_tok] = 0
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    topk = dsa.dsa_indexer_topk(wl.q_idx.to(dev), wl.w.to(dev), wl.kcache[0].to(dev), *meta_to(rg, dev),
+                                k=wl.k, max_kv=rg.max_kv, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    T = rg.T
+    sample = sorted(set(zero_tok) | {0, 1, n_per // 2, n_per - 2, n_per, n_per + 1, T // 2 + 7, T - 1}
+                    | set(np.random.default_rng(3).choice(T, 8, replace=False).tolist()))
+    ref, srows = O.indexer_topk(f32(wl.q_idx), f32(wl.w), f32(wl.kcache[0]), **meta_np(rg), k=wl.k,
+                                tokens=np.asarray(sample))
+    got = topk.cpu().numpy()[sample]
+    check_topk_rows(got, ref, wl.k, srows)
+    for i, t in enumerate(sample):
+        if t in zero_tok:
+            assert np.array_equal(got[i], np.arange(wl.k))  # all-tie rows: the lowest k positions
+        if t >= n_per:
+            assert np.array_equal(got[i], ref[i])  # four distinct values: no near-tie freedom
