@@ -7,14 +7,17 @@
 // K* and how many copies of K* are needed; a final pass of warp ballots and
 // two block scans emits every index with key > K* plus the lowest-index
 // copies of K*, already in ascending order. Rows that fit are first staged in
-// shared memory; longer rows are re-read from global memory (L2) per pass.
+// shared memory. Longer rows are read once: a threshold from a strided
+// sample of the row bounds a candidate list that then takes the select; when
+// the sample misleads (fewer than k or too many candidates) a two-read path
+// with an 11-bit histogram, and last a path that re-reads the row from L2 per
+// radix pass, take over.
 #include "common.cuh"
 #include "indexer.cuh"
 
 namespace dsa {
 
 constexpr int kTopkThreads = 512;
-constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kTopkThreadsShort = 128;  // threads per row when every row has at most kTopkShortCap keys
 constexpr int kTopkShortCap = 8192;
 constexpr int kTopkThreadsMany = 256;   // threads per row for many rows of any length
@@ -291,6 +294,41 @@ __device__ void select_row_global(const float* __restrict__ g, int n, int k, int
   }
 }
 
+// The key of rank `rank` (1 = largest) among m ordered keys in shared
+// memory, by a 4-pass radix select; `remaining` returns how many copies of
+// that key belong to the top `rank`. Block-wide.
+template <int TPB>
+__device__ uint32_t rank_key(const uint32_t* __restrict__ keys, int m, int rank, uint32_t* hist, int& remaining) {
+  constexpr int W = TPB / 32;
+  __shared__ int s_sel[2];
+  const int tid = threadIdx.x, w = warp_id();
+  uint32_t prefix = 0, mask = 0;
+  remaining = rank;
+  const int mround = (m + TPB - 1) / TPB * TPB;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = tid; i < W * 256; i += TPB) hist[i] = 0;
+    __syncthreads();
+    uint32_t* wh = hist + w * 256;
+    for (int i = tid; i < mround; i += TPB) hist_add(wh, i < m ? keys[i] : 0u, i < m, prefix, mask, shift);
+    __syncthreads();
+    pick_digit<TPB>(hist, shift, prefix, mask, remaining, s_sel);
+  }
+  return prefix;
+}
+
+// Exact top-k of a row from a candidate list in shared memory (ordered keys
+// ckey and row positions cidx, ascending in position) that holds every
+// winner: the rank-k key, then the ordered emission over the list.
+template <int TPB>
+__device__ void select_candidates(const float* __restrict__ g, const uint32_t* __restrict__ ckey,
+                                  const int* __restrict__ cidx, int m, int k, int32_t* __restrict__ out_idx,
+                                  float* __restrict__ out_val, uint32_t* hist, int* s_tmp) {
+  int remaining;
+  const uint32_t kstar = rank_key<TPB>(ckey, m, k, hist, remaining);
+  emit_ordered<true, TPB>(g, ckey, m, kstar, remaining, out_idx, out_val, s_tmp, cidx);
+}
+
 // Row longer than shared memory, in two reads of the row instead of one per
 // radix digit:
 //  A. every warp histograms the top kWideBits bits of the keys of its own
@@ -455,20 +493,134 @@ __device__ bool select_row_two_pass(const float* __restrict__ g, int n, int k, i
     }
   }
   __syncthreads();
-  // ---- C: exact radix select of rank k among the m candidates
-  uint32_t prefix = 0, mask = 0;
-  int remaining = k;
-  const int mround = (m + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = tid; i < kTopkWarps * 256; i += kTopkThreads) hist[i] = 0;
+  // ---- C
+  select_candidates<TPB>(g, ckey, cidx, m, k, out_idx, out_val, hist, s_tmp);
+  return true;
+}
+
+// Row longer than shared memory, in one read: a threshold t0 from a strided
+// sample of the row bounds the candidates.
+//  A. kSample keys at evenly spaced positions; t0 = the sample's key of rank
+//     r, r chosen so that about (k + capacity) / 2 keys of the row are
+//     expected at or above t0 (halfway between too few and too many);
+//  B. one pass over the row in block-wide chunks copies every key >= t0,
+//     in position order, into the candidate list (per chunk, each warp takes
+//     a contiguous run; a scan over the warps gives the offsets);
+//  C. if at least k keys were copied, the k-th largest key is >= t0, so the
+//     list holds every winner: exact select and ordered emission on it.
+// Returns false (before writing anything) when fewer than k or more than the
+// list capacity were found (massive ties, unusual score distributions); the
+// caller then takes the two-pass path.
+constexpr int kSample = 1024;
+constexpr int kAhead = 2;  // chunks of the row prefetched into L2 ahead of the pass
+
+template <int TPB>
+__device__ bool select_row_sampled(const float* __restrict__ g, int n, int k, int32_t* __restrict__ out_idx,
+                                   float* __restrict__ out_val, uint32_t* hist, uint32_t* area, int* s_tmp) {
+  constexpr int W = TPB / 32;
+  constexpr int kCandCap = stage_cap<TPB>() / 2;
+  static_assert(kSample <= kCandCap, "the sample fits the candidate list");
+  if (2 * k > kCandCap) return false;  // a list of (k + cap) / 2 expected entries would crowd the cap
+  const int tid = threadIdx.x, w = warp_id(), lane = lane_id();
+  __shared__ int s_wcnt[2][W];
+  const int n4 = (n + 3) / 4;
+  const float4* g4 = reinterpret_cast<const float4*>(g);
+  constexpr int U = 4;                  // float4 groups per lane per chunk
+  constexpr int kChunk4 = TPB * U;      // float4 groups per chunk
+  // the first chunks of the row start their way into L2 under the sample
+  // (one 128-byte line per prefetch, kAhead chunks ahead of the pass)
+  auto prefetch_chunk = [&](int c0) {
+    for (int l = tid; l < kChunk4 / 8; l += TPB) {
+      const int i4 = c0 + 8 * l;
+      if (i4 < n4) prefetch_l2(g4 + i4);
+    }
+  };
+#pragma unroll 1
+  for (int c = 0; c < kAhead; ++c) prefetch_chunk(c * kChunk4);
+  // ---- A
+  uint32_t* skey = area;
+  for (int j = tid; j < kSample; j += TPB) skey[j] = ordered_key(__ldg(g + (int)(((long long)j * n) / kSample)));
+  __syncthreads();
+  const long long target = min(2LL * k, (long long)(k + kCandCap) / 2);
+  const int r = (int)max(1LL, min((long long)kSample, (target * kSample + n / 2) / n));
+  int rem_unused;
+  const uint32_t t0 = rank_key<TPB>(skey, kSample, r, hist, rem_unused);
+  __syncthreads();  // the sample is dead: the area holds the list
+  uint32_t* ckey = area;
+  int* cidx = reinterpret_cast<int*>(area + kCandCap);
+  // ---- B
+  int run = 0;                          // candidates before this chunk (block-uniform)
+  float4 v[U];
+  auto load = [&](int c0) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i4 = c0 + w * 32 * U + u * 32 + lane;
+      v[u] = i4 < n4 ? __ldg(g4 + i4) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+  };
+  load(0);
+  for (int c0 = 0, par = 0; c0 < n4; c0 += kChunk4, par ^= 1) {
+    uint32_t fl[U];  // per group: bit cc set when position 4*i4 + cc is a candidate
+    uint32_t key[U][4];
+    int wtot = 0;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = 4 * (c0 + w * 32 * U + u * 32 + lane);
+      const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      fl[u] = 0;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        key[u][cc] = ordered_key(e[cc]);
+        if (i + cc < n && key[u][cc] >= t0) fl[u] |= 1u << cc;
+      }
+      wtot += __popc(fl[u]);
+    }
+    if (c0 + kChunk4 < n4) load(c0 + kChunk4);  // the next chunk's loads fly during the scans
+    prefetch_chunk(c0 + kAhead * kChunk4);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wtot += __shfl_xor_sync(0xffffffffu, wtot, o);
+    if (lane == 0) s_wcnt[par][w] = wtot;
     __syncthreads();
-    uint32_t* wh = hist + w * 256;
-    for (int i = tid; i < mround; i += kTopkThreads) hist_add(wh, i < m ? ckey[i] : 0u, i < m, prefix, mask, shift);
-    __syncthreads();
-    pick_digit<TPB>(hist, shift, prefix, mask, remaining, s_sel);
+    int woff = run, ctot = 0;
+#pragma unroll
+    for (int ww = 0; ww < W; ++ww) {
+      const int c = s_wcnt[par][ww];
+      woff += ww < w ? c : 0;
+      ctot += c;
+    }
+    // lanes hold consecutive groups of four positions: an exclusive scan of
+    // the per-lane counts keeps the list in position order
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = __popc(fl[u]);
+      int xs = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, xs, o);
+        if (lane >= o) xs += y;
+      }
+      int pos = woff + xs - c;
+      const int i = 4 * (c0 + w * 32 * U + u * 32 + lane);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        if ((fl[u] >> cc) & 1u) {
+          if (pos < kCandCap) {
+            ckey[pos] = key[u][cc];
+            cidx[pos] = i + cc;
+          }
+          ++pos;
+        }
+      }
+      woff += __shfl_sync(0xffffffffu, xs, 31);
+    }
+    run += ctot;
+    // s_wcnt alternates between two buffers: the next chunk's counts never
+    // overwrite ones a slower warp is still reading
   }
-  emit_ordered<true, TPB>(g, ckey, m, prefix, remaining, out_idx, out_val, s_tmp, cidx);
+  __syncthreads();
+  if (run < k || run > kCandCap) return false;  // uniform over the block
+  // ---- C
+  select_candidates<TPB>(g, ckey, cidx, run, k, out_idx, out_val, hist, s_tmp);
   return true;
 }
 
@@ -551,7 +703,8 @@ __global__ void __launch_bounds__(TPB, TPB == kTopkThreadsMany ? 3 : 1)
     __syncthreads();
     select_row_staged<TPB>(g, s_row, n, k, oi, ov, hist, s_tmp);
   } else if constexpr (TPB != kTopkThreadsShort) {
-    if (cap < stage_cap<TPB>() || !select_row_two_pass<TPB>(g, n, k, oi, ov, hist, s_row, s_tmp))
+    if (cap < stage_cap<TPB>() || (!select_row_sampled<TPB>(g, n, k, oi, ov, hist, s_row, s_tmp) &&
+                                   !select_row_two_pass<TPB>(g, n, k, oi, ov, hist, s_row, s_tmp)))
       select_row_global<TPB>(g, n, k, oi, ov, hist, s_tmp, reinterpret_cast<int*>(s_row), cap / 2);
   }
   // (the short-row instantiation is only launched when every row fits cap)

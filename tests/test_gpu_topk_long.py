@@ -115,3 +115,31 @@ def test_many_long_rows_token_topk(dsa):
             assert np.array_equal(got[i], np.arange(wl.k))  # all-tie rows: the lowest k positions
         if t >= n_per:
             assert np.array_equal(got[i], ref[i])  # four distinct values: no near-tie freedom
+
+
+def test_long_rows_sample_misleads(dsa):
+    """A row whose evenly spaced positions (the ones a strided sample of the
+    row sees) hold its largest scores: a threshold taken from such a sample
+    admits fewer than k keys, and the selection must still be exact."""
+    dev = torch.device("cuda")
+    n = 40960
+    wl = DI.random_small(81, [1, 1], [n, 37000], H=16, k=2048)
+    rg = wl.rg
+    ps = rg.page_size
+    kc = wl.kcache[0].view(-1, 128)
+    qsum = wl.q_idx[0].float().sum(0)
+    v = (qsum / qsum.norm() * 16).to(torch.bfloat16)
+    planted = np.arange(0, n, n // 1024)
+    base = int(rg.cu_kv_lens[0]) // ps
+    rows = rg.page_indices[base + planted // ps].astype(np.int64) * ps + planted % ps
+    kc[torch.from_numpy(rows)] = v
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    topk = dsa.dsa_indexer_topk(wl.q_idx.to(dev), wl.w.to(dev), wl.kcache[0].to(dev), *meta_to(rg, dev),
+                                k=wl.k, max_kv=rg.max_kv, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    ref, srows = O.indexer_topk(f32(wl.q_idx), f32(wl.w), f32(wl.kcache[0]), **meta_np(rg), k=wl.k)
+    # the planted positions are the row's 1024 largest scores
+    assert set(np.argsort(-srows[0].astype(np.float64), kind="stable")[:1024].tolist()) == set(planted.tolist())
+    got = topk.cpu().numpy()
+    check_topk_rows(got, ref, wl.k, srows)
