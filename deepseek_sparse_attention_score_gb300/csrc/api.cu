@@ -112,8 +112,9 @@ static int indexer_common(cudaStream_t stream, const uint16_t* q, const float* w
     if (rc) return rc;
   }
   if (topk_pages) {
-    rc = run_topk(stream, out.page_scores, out.ld_pg, pl.nvis, T, ps, k_pages, topk_pages, nullptr,
-                  (max_kv + ps - 1) / ps);
+    rc = run_page_topk(stream, out.gran_scores, out.ld_gr, pl.nvis, T, ps, k_pages, topk_pages,
+                       reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.page_scores), (long long)L.ld_pg,
+                       (max_kv + ps - 1) / ps);
     if (rc) return rc;
   }
   return DSA_OK;

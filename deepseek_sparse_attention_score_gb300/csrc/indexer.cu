@@ -175,10 +175,7 @@ struct IdxCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_STAGE = 2 * Q_BYTES;
   static constexpr int OFF_W = OFF_STAGE + STAGES * STAGE_BYTES;
-  static constexpr int OFF_PMAX = OFF_W + 2 * N * 4;
-  // page max-pool slots {ordered key, arrivals} per (tile mod 4, query, page of the tile)
-  static constexpr int PM_SLOTS = 4 * NQ * 2;
-  static constexpr int OFF_BAR = OFF_PMAX + PM_SLOTS * 8;
+  static constexpr int OFF_BAR = OFF_W + 2 * N * 4;
   static constexpr int NBAR = 2 * STAGES + 9;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
@@ -213,8 +210,6 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::THREADS, 1)
   uint8_t* q_s = smem + C::OFF_Q;
   uint8_t* st_s = smem + C::OFF_STAGE;
   float* w_s = reinterpret_cast<float*>(smem + C::OFF_W);
-  uint32_t* pm_key = reinterpret_cast<uint32_t*>(smem + C::OFF_PMAX);
-  uint32_t* pm_cnt = pm_key + C::PM_SLOTS;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::STAGES;
@@ -241,7 +236,6 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::THREADS, 1)
     }
     mbar_init(fin, 1);
     *abort_flag = 0;
-    for (int i = 0; i < 2 * C::PM_SLOTS; ++i) pm_key[i] = 0u;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -379,7 +373,6 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::THREADS, 1)
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int qset = ew >> 2;
     constexpr int QPW = C::QPW;
-    const int ps = m.ps;
     int dt = 0, it = 0;
     bool ok = true;
     for (int ii = blockIdx.x; ii < n_items && ok; ii += gridDim.x, ++it) {
@@ -431,31 +424,13 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::THREADS, 1)
           const float sc = (s0 + s1) + (s2 + s3);
           const bool valid = key >= kb && key < ke && key < nv[j];
           if (out.tok_scores && valid) out.tok_scores[(size_t)(t0 + q) * out.ld_tok + key] = sc;
-          if (out.page_scores) {
+          if (out.gran_scores) {
+            // the maximum of this quadrant's 32 keys: one granule (a page
+            // of ps keys is ps / 32 granules, folded by the page top-k)
             const float pm = warp_max_f32(valid ? sc : -INFINITY);
             const int qkey0 = tile * 128 + quad * 32;  // first key of this quadrant
-            if (ps == 32) {
-              if (lane == 0 && qkey0 < nv[j] && qkey0 >= kb)
-                out.page_scores[(size_t)(t0 + q) * out.ld_pg + qkey0 / 32] = pm;
-            } else if (lane == 0) {
-              // a page spans ps / 32 quadrants (warps): each folds its maximum
-              // into the page's slot; the last to arrive writes the page score
-              // and clears the slot. A warp runs at most two tiles ahead of
-              // the slowest one (the D buffers hold it), so slots rotate over
-              // four tiles.
-              const int qpp = ps / 32, pg = quad / qpp;
-              const int slot = (((dt & 3) * NQ + q) * 2) + pg;
-              atomicMax(pm_key + slot, ordered_key_f32(pm));
-              __threadfence_block();
-              if (atomicAdd(pm_cnt + slot, 1u) == (uint32_t)(qpp - 1)) {
-                __threadfence_block();
-                const uint32_t mk = atomicExch(pm_key + slot, 0u);
-                atomicExch(pm_cnt + slot, 0u);
-                const int key0 = tile * 128 + pg * ps;
-                if (key0 < nv[j] && key0 < ke && key0 >= kb)
-                  out.page_scores[(size_t)(t0 + q) * out.ld_pg + key0 / ps] = ordered_key_value(mk);
-              }
-            }
+            if (lane == 0 && qkey0 < nv[j] && qkey0 >= kb)
+              out.gran_scores[(size_t)(t0 + q) * out.ld_gr + qkey0 / 32] = pm;
           }
         }
       }
@@ -493,8 +468,10 @@ IndexerLayout indexer_layout(int T, int S, int max_kv, int ps) {
   L.dec_items = take((size_t)(dec_tiles * nchunk1) * 16);
   L.pre_items = take((size_t)(pre_tiles * nchunk8) * 16);
   L.ld_tok = align_up((size_t)max_kv, 128);
+  L.ld_gr = align_up((size_t)(max_kv + 31) / 32, 4);
   L.ld_pg = align_up((size_t)(max_kv + ps - 1) / ps, 4);
   L.tok_scores = take((size_t)T * L.ld_tok * 4);
+  L.gran_scores = take((size_t)T * L.ld_gr * 4);
   L.page_scores = take((size_t)T * L.ld_pg * 4);
   L.total = off;
   return L;
@@ -513,9 +490,9 @@ int run_indexer(cudaStream_t stream, const IndexerMeta& m, const uint16_t* q, co
   pl.pre_items = reinterpret_cast<int4*>(base + L.pre_items);
   IndexerOut out;
   out.tok_scores = want_tok ? reinterpret_cast<float*>(base + L.tok_scores) : nullptr;
-  out.page_scores = want_page ? reinterpret_cast<float*>(base + L.page_scores) : nullptr;
+  out.gran_scores = want_page ? reinterpret_cast<float*>(base + L.gran_scores) : nullptr;
   out.ld_tok = (long long)L.ld_tok;
-  out.ld_pg = (long long)L.ld_pg;
+  out.ld_gr = (long long)L.ld_gr;
   *plan_out = pl;
   *out_out = out;
   if (m.T == 0) return DSA_OK;

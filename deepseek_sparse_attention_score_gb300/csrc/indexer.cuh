@@ -32,13 +32,15 @@ struct IndexerPlan {
 
 struct IndexerOut {
   float* tok_scores;   // [T, ld_tok] or null
-  float* page_scores;  // [T, ld_pg] or null
-  long long ld_tok, ld_pg;
+  float* gran_scores;  // [T, ld_gr] or null: the maximum score of every 32-key granule
+  long long ld_tok, ld_gr;
 };
 
+// page_scores [T, ld_pg]: page maxima folded from the granules, only for page
+// rows longer than the page top-k can fold while it reads them
 struct IndexerLayout {
-  size_t counts, nvis, seq_tile_off, dec_tiles, pre_tiles, dec_items, pre_items, tok_scores, page_scores;
-  size_t ld_tok, ld_pg, total;
+  size_t counts, nvis, seq_tile_off, dec_tiles, pre_tiles, dec_items, pre_items, tok_scores, gran_scores, page_scores;
+  size_t ld_tok, ld_gr, ld_pg, total;
 };
 
 IndexerLayout indexer_layout(int T, int S, int max_kv, int ps);
@@ -52,5 +54,10 @@ int run_topk_approx(cudaStream_t stream, const float* scores, long long ld, cons
 // Exact per-row top-k over a score buffer (token or page scores).
 int run_topk(cudaStream_t stream, const float* scores, long long ld, const int* nvis, int T, int div, int k,
              int32_t* out_idx, float* out_val, int max_len);
+// Exact page top-k from 32-key granule maxima: a page's score is the maximum
+// of its ps / 32 visible granules. page_buf [T, ld_pg] is used only when the
+// rows are too long to fold while reading.
+int run_page_topk(cudaStream_t stream, const float* gran, long long ld_gr, const int* nvis, int T, int ps, int k_pages,
+                  int32_t* out_idx, float* page_buf, long long ld_pg, int max_pages);
 
 }  // namespace dsa

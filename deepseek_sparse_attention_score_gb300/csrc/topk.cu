@@ -29,6 +29,24 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// Page score from 32-key granule maxima: unit i of a row covers granules
+// fold*i .. fold*i + fold - 1 (fold = 2 or 4), of which only those starting
+// below the row's visible length nraw hold scores. The row starts 16-byte
+// aligned and its stride is a multiple of four granules.
+__device__ __forceinline__ float fold_max(const float* __restrict__ g, int i, int fold, int nraw) {
+  const int g0 = i * fold;
+  if (fold == 2) {
+    const float2 a = __ldg(reinterpret_cast<const float2*>(g) + i);
+    return 32 * (g0 + 1) < nraw ? fmaxf(a.x, a.y) : a.x;
+  }
+  const float4 a = __ldg(reinterpret_cast<const float4*>(g) + i);
+  float mx = a.x;
+  if (32 * (g0 + 1) < nraw) mx = fmaxf(mx, a.y);
+  if (32 * (g0 + 2) < nraw) mx = fmaxf(mx, a.z);
+  if (32 * (g0 + 3) < nraw) mx = fmaxf(mx, a.w);
+  return mx;
+}
+
 template <int TPB>
 __device__ __forceinline__ int block_scan_warps(int v, int* s_tmp, int* total) {
   // exclusive scan of one value per warp (lane 0 holds it) across the block
@@ -295,17 +313,47 @@ __device__ void select_row_global(const float* __restrict__ g, int n, int k, int
 }
 
 // The key of rank `rank` (1 = largest) among m ordered keys in shared
-// memory, by a 4-pass radix select; `remaining` returns how many copies of
-// that key belong to the top `rank`. Block-wide.
+// memory, by a most-significant-digit radix select; `remaining` returns how
+// many copies of that key belong to the top `rank`. Digits above the first
+// bit in which the keys differ are skipped (a candidate list near the top of
+// a row shares its leading digits, and a pass over one shared digit would
+// send every atomic of a warp to one bin). With last_pass < 3 the select
+// stops after that digit and returns the lower bound of the bin that holds
+// the rank-`rank` key (at most that key). Block-wide.
 template <int TPB>
-__device__ uint32_t rank_key(const uint32_t* __restrict__ keys, int m, int rank, uint32_t* hist, int& remaining) {
+__device__ uint32_t rank_key(const uint32_t* __restrict__ keys, int m, int rank, uint32_t* hist, int& remaining,
+                             int last_pass = 3) {
   constexpr int W = TPB / 32;
   __shared__ int s_sel[2];
-  const int tid = threadIdx.x, w = warp_id();
-  uint32_t prefix = 0, mask = 0;
+  __shared__ uint32_t s_ao[2][W];
+  const int tid = threadIdx.x, w = warp_id(), lane = lane_id();
+  uint32_t a = 0xffffffffu, o = 0u;
+  for (int i = tid; i < m; i += TPB) {
+    a &= keys[i];
+    o |= keys[i];
+  }
+  a = __reduce_and_sync(0xffffffffu, a);
+  o = __reduce_or_sync(0xffffffffu, o);
+  if (lane == 0) {
+    s_ao[0][w] = a;
+    s_ao[1][w] = o;
+  }
+  __syncthreads();
+  a = 0xffffffffu;
+  o = 0u;
+#pragma unroll
+  for (int ww = 0; ww < W; ++ww) {
+    a &= s_ao[0][ww];
+    o |= s_ao[1][ww];
+  }
   remaining = rank;
+  const uint32_t diff = a ^ o;
+  if (diff == 0u) return a;  // every key is equal (m > 0)
+  const int first = __clz(diff) >> 3;  // the first digit in which keys differ
+  uint32_t mask = first ? ~0u << (32 - 8 * first) : 0u;
+  uint32_t prefix = a & mask;
   const int mround = (m + TPB - 1) / TPB * TPB;
-  for (int pass = 0; pass < 4; ++pass) {
+  for (int pass = first; pass <= last_pass; ++pass) {
     const int shift = 24 - 8 * pass;
     for (int i = tid; i < W * 256; i += TPB) hist[i] = 0;
     __syncthreads();
@@ -544,7 +592,10 @@ __device__ bool select_row_sampled(const float* __restrict__ g, int n, int k, in
   const long long target = min(2LL * k, (long long)(k + kCandCap) / 2);
   const int r = (int)max(1LL, min((long long)kSample, (target * kSample + n / 2) / n));
   int rem_unused;
-  const uint32_t t0 = rank_key<TPB>(skey, kSample, r, hist, rem_unused);
+  // two digits resolve t0 to its 16-bit bin (sign, exponent and seven
+  // mantissa bits): t0 is that bin's lower bound, a little below the sample's
+  // rank-r key, which only adds the keys within the bin
+  const uint32_t t0 = rank_key<TPB>(skey, kSample, r, hist, rem_unused, 1);
   __syncthreads();  // the sample is dead: the area holds the list
   uint32_t* ckey = area;
   int* cidx = reinterpret_cast<int*>(area + kCandCap);
@@ -656,7 +707,7 @@ __device__ void select_row_staged(const float* __restrict__ g, const uint32_t* _
 template <int TPB>
 __global__ void __launch_bounds__(TPB, TPB == kTopkThreadsMany ? 3 : 1)
     topk_rows_kernel(const float* __restrict__ scores, long long ld, const int* __restrict__ nvis, int div, int k,
-                     int32_t* __restrict__ out_idx, float* __restrict__ out_val, int cap) {
+                     int32_t* __restrict__ out_idx, float* __restrict__ out_val, int cap, int fold) {
   constexpr int W = TPB / 32;
   griddep_launch_dependents();
   griddep_wait();
@@ -665,7 +716,8 @@ __global__ void __launch_bounds__(TPB, TPB == kTopkThreadsMany ? 3 : 1)
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem);  // (warps + 1) * 256
   uint32_t* s_row = hist + (W + 1) * 256;               // cap keys
   const int row = blockIdx.x;
-  int n = nvis[row];
+  const int nraw = nvis[row];
+  int n = nraw;
   if (div > 1) n = (n + div - 1) / div;
   const float* g = scores + (size_t)row * ld;
   int32_t* oi = out_idx + (size_t)row * k;
@@ -688,7 +740,7 @@ __global__ void __launch_bounds__(TPB, TPB == kTopkThreadsMany ? 3 : 1)
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int i = b0 + u * TPB + threadIdx.x;
-        v[u] = i < n ? __ldg(g + i) : 0.f;
+        v[u] = i >= n ? 0.f : fold == 1 ? __ldg(g + i) : fold_max(g, i, fold, nraw);
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -710,8 +762,23 @@ __global__ void __launch_bounds__(TPB, TPB == kTopkThreadsMany ? 3 : 1)
   // (the short-row instantiation is only launched when every row fits cap)
 }
 
-int run_topk(cudaStream_t stream, const float* scores, long long ld, const int* nvis, int T, int div, int k,
-             int32_t* out_idx, float* out_val, int max_len) {
+// The block size for a launch: short blocks pay off when their extra rows
+// per SM are there to fill it (many rows) or the rows are short; a few long
+// rows keep the wide block (measured: 32 rows of 4-8 K keys took 61 us with
+// short blocks, 41 us wide).
+static int topk_tier(int T, int max_len) {
+  const bool many = T >= 2 * sm_count();
+  if (max_len <= kTopkShortCap && (many || max_len <= 2048)) return kTopkThreadsShort;
+  return many ? kTopkThreadsMany : kTopkThreads;
+}
+
+static int topk_stage_cap(int tpb) {
+  return tpb == kTopkThreadsShort ? stage_cap<kTopkThreadsShort>()
+         : tpb == kTopkThreadsMany ? stage_cap<kTopkThreadsMany>() : stage_cap<kTopkThreads>();
+}
+
+static int launch_topk(cudaStream_t stream, const float* scores, long long ld, const int* nvis, int T, int div, int k,
+                       int32_t* out_idx, float* out_val, int max_len, int fold) {
   if (T == 0) return DSA_OK;
   // rows longer than the staging capacity are read as float4: every row must
   // start 16-byte aligned
@@ -727,17 +794,49 @@ int run_topk(cudaStream_t stream, const float* scores, long long ld, const int* 
     set_smem_attr_once(reinterpret_cast<const void*>(topk_rows_kernel<TPB>),
                        (W + 1) * 256 * 4 + stage_cap<TPB>() * 4);
     DSA_LAUNCH_PDL(topk_rows_kernel<TPB>, dim3(T), dim3(TPB), smem, stream, scores, ld, nvis, div, k, out_idx,
-                   out_val, cap);
+                   out_val, cap, fold);
     return DSA_OK;
   };
-  const bool many = T >= 2 * sm_count();
-  // short blocks pay off when their extra rows per SM are there to fill it
-  // (many rows) or the rows are short; a few long rows keep the wide block
-  // (measured: 32 rows of 4-8 K keys took 61 us with short blocks, 41 us wide)
-  if (max_len <= kTopkShortCap && (many || max_len <= 2048))
-    return launch(std::integral_constant<int, kTopkThreadsShort>{});
-  if (many) return launch(std::integral_constant<int, kTopkThreadsMany>{});
+  const int tier = topk_tier(T, max_len);
+  if (tier == kTopkThreadsShort) return launch(std::integral_constant<int, kTopkThreadsShort>{});
+  if (tier == kTopkThreadsMany) return launch(std::integral_constant<int, kTopkThreadsMany>{});
   return launch(std::integral_constant<int, kTopkThreads>{});
+}
+
+int run_topk(cudaStream_t stream, const float* scores, long long ld, const int* nvis, int T, int div, int k,
+             int32_t* out_idx, float* out_val, int max_len) {
+  return launch_topk(stream, scores, ld, nvis, T, div, k, out_idx, out_val, max_len, 1);
+}
+
+// page maxima from granule maxima, for page rows longer than a stage
+__global__ void fold_pages_kernel(const float* __restrict__ gran, long long ld_gr, const int* __restrict__ nvis, int T,
+                                  int ps, float* __restrict__ pages, long long ld_pg, int max_pages) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int fold = ps / 32;
+  const long long total = (long long)T * max_pages;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(e / max_pages), i = (int)(e % max_pages);
+    const int nraw = nvis[t];
+    if ((long long)i * ps < nraw) pages[(size_t)t * ld_pg + i] = fold_max(gran + (size_t)t * ld_gr, i, fold, nraw);
+  }
+}
+
+int run_page_topk(cudaStream_t stream, const float* gran, long long ld_gr, const int* nvis, int T, int ps, int k_pages,
+                  int32_t* out_idx, float* page_buf, long long ld_pg, int max_pages) {
+  if (T == 0) return DSA_OK;
+  const int fold = ps / 32;
+  if (fold == 1) return launch_topk(stream, gran, ld_gr, nvis, T, ps, k_pages, out_idx, nullptr, max_pages, 1);
+  // staged rows fold their granules while they are staged; longer rows take
+  // a folding pass first
+  if (max_pages <= topk_stage_cap(topk_tier(T, max_pages)))
+    return launch_topk(stream, gran, ld_gr, nvis, T, ps, k_pages, out_idx, nullptr, max_pages, fold);
+  if ((ld_gr & 3) || (reinterpret_cast<uintptr_t>(gran) & 15)) return DSA_ERR_ALIGNMENT;
+  const long long total = (long long)T * max_pages;
+  const int blocks = (int)std::min<long long>((total + 255) / 256, 8LL * sm_count());
+  DSA_LAUNCH_PDL(fold_pages_kernel, dim3(blocks), dim3(256), 0, stream, gran, ld_gr, nvis, T, ps, page_buf, ld_pg,
+                 max_pages);
+  return launch_topk(stream, page_buf, ld_pg, nvis, T, ps, k_pages, out_idx, nullptr, max_pages, 1);
 }
 
 }  // namespace dsa

@@ -59,7 +59,7 @@ def test_indexer_token_topk(dsa, case, ps):
 
 
 @pytest.mark.parametrize("case", list(CASES))
-@pytest.mark.parametrize("ps", [64, 32])
+@pytest.mark.parametrize("ps", [64, 32, 128])
 def test_indexer_page_topk(dsa, case, ps):
     dev = torch.device("cuda")
     wl = _wl(case, 200 + len(case) + ps, ps=ps, k=48, k_pages=3)

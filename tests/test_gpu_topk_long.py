@@ -143,3 +143,62 @@ def test_long_rows_sample_misleads(dsa):
     assert set(np.argsort(-srows[0].astype(np.float64), kind="stable")[:1024].tolist()) == set(planted.tolist())
     got = topk.cpu().numpy()
     check_topk_rows(got, ref, wl.k, srows)
+
+
+@pytest.mark.parametrize("full_pages", [600, 34380])
+def test_page_topk_folds_visible_granules(dsa, full_pages):
+    """Page scores are folded from 32-key granule maxima. A page whose tail is
+    not visible must ignore the granules past the visible length even when
+    the workspace still holds larger values there from an earlier call with a
+    longer row. With 34 380 full pages the rows exceed every shared-memory
+    stage (a folding pass runs first); with 600 they are folded while staged.
+    Keys are zero except planted copies of two vectors A and B = A / 2, so
+    the expected selection follows from the oracle's scores of A and B."""
+    dev = torch.device("cuda")
+    ps, k_pages, seed = 64, 16, 83
+    n_long, n_short = full_pages * ps + 60, full_pages * ps + 20  # same page count
+    q_lens = [1, 1, 1, 1]
+    rgs = [DI.make_ragged(q_lens, [n, 1000, 1500, 700], ps, master_seed=seed, spare_pages=2)
+           for n in (n_long, n_short)]
+    assert np.array_equal(rgs[0].page_indices, rgs[1].page_indices)
+    T, P = 4, rgs[0].num_pages
+    q_idx = DI.randn((T, DI.INDEX_HEADS, DI.INDEX_DIM), seed, "q_idx").to(torch.bfloat16)
+    w = DI.rand((T, DI.INDEX_HEADS), seed, "w") / np.sqrt(DI.INDEX_HEADS)
+    qs = q_idx[0].float().sum(0)
+    A = (qs / qs.norm() * 16).to(torch.bfloat16)
+    B = (A.float() * 0.5).to(torch.bfloat16)
+    sA, sB = O.indexer_score_row(f32(q_idx[0]), f32(w[0]), f32(torch.stack([A, B])))
+    assert sA > sB > 0
+    # request 0: zero keys with planted A / B keys; the other requests' keys N(0,1)
+    pi = rgs[0].page_indices
+    last = full_pages  # index of request 0's partly visible page
+    kc = torch.zeros((P, ps, DI.INDEX_DIM), dtype=torch.bfloat16)
+    rest = torch.from_numpy(pi[last + 1:].astype(np.int64))
+    kc[rest] = DI.randn((len(rest), ps, DI.INDEX_DIM), seed, "kcache").to(torch.bfloat16)
+    pa = [5, full_pages // 2, full_pages - 1]
+    pb = sorted(set(np.linspace(1, full_pages - 2, 40).astype(int).tolist()) - set(pa))
+    for p in pa:
+        kc[int(pi[p]), 7] = A
+    for p in pb:
+        kc[int(pi[p]), 33] = B
+    kc[int(pi[last]), 45] = A  # visible at n_long (offset 45 < 60), past n_short (45 >= 20)
+    kcd = kc.to(dev)
+    ws = torch.empty(dsa.dsa_indexer_workspace_size(T, 4, n_long, ps), dtype=torch.uint8, device=dev)
+    got = []
+    for rg in rgs:
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        pages = dsa.dsa_indexer_page_topk(q_idx.to(dev), w.to(dev), kcd, *meta_to(rg, dev), k_pages=k_pages,
+                                          max_kv=n_long, ws=ws, dev_status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        got.append(pages.cpu().numpy())
+    # request 0: the A pages, then the lowest-index B pages (ties to the lower index)
+    want_long = sorted(pa + [last] + pb[: k_pages - len(pa) - 1])
+    want_short = sorted(pa + pb[: k_pages - len(pa)])
+    assert got[0][0].tolist() == want_long
+    assert got[1][0].tolist() == want_short
+    # requests 1..3 against the oracle's page top-k
+    ref, srows = O.indexer_page_topk(f32(q_idx), f32(w), kc.view(torch.int16).numpy(), **meta_np(rgs[1]),
+                                     k_pages=k_pages, tokens=np.arange(1, T))
+    prow = [O.page_scores_of_row(r, ps) for r in srows]
+    check_topk_rows(got[1][1:], ref, k_pages, prow, what="page top-k")
