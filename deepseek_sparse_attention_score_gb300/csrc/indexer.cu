@@ -46,7 +46,11 @@ __device__ int block_excl_scan(int v, int* s_warp, int* total) {
 
 constexpr int kPlanStageS = 4096;  // requests whose query offsets the planner keeps in shared memory
 
-__global__ void __launch_bounds__(1024) indexer_plan_kernel(IndexerMeta m, IndexerPlan pl, int ch1, int ch8) {
+// one_token: every token becomes a one-token tile (the launch has as many
+// tokens as requests, so it is a decode batch but for requests without new
+// tokens; the eight-query kernel is then not launched at all)
+__global__ void __launch_bounds__(1024) indexer_plan_kernel(IndexerMeta m, IndexerPlan pl, int ch1, int ch8,
+                                                            int one_token) {
   griddep_launch_dependents();
   griddep_wait();
   __shared__ int s_warp[32];
@@ -91,7 +95,9 @@ __global__ void __launch_bounds__(1024) indexer_plan_kernel(IndexerMeta m, Index
     int nd = 0, np = 0;
     if (s < S) {
       const int ql = staged ? s_cuq[s + 1] - s_cuq[s] : __ldg(m.cu_q_lens + s + 1) - __ldg(m.cu_q_lens + s);
-      if (ql > 0) {
+      if (ql > 0 && one_token) {
+        nd = ql;
+      } else if (ql > 0) {
         const int nt = (ql + 7) / 8;
         nd = (ql - 8 * (nt - 1)) == 1 ? 1 : 0;
         np = nt - nd;
@@ -112,10 +118,14 @@ __global__ void __launch_bounds__(1024) indexer_plan_kernel(IndexerMeta m, Index
     const int q0 = staged ? s_cuq[s] : __ldg(m.cu_q_lens + s);
     const int ql = (staged ? s_cuq[s + 1] : __ldg(m.cu_q_lens + s + 1)) - q0;
     const int r = t - q0;
+    const int2 off = pl.seq_tile_off[s];
+    if (one_token) {
+      pl.dec_tiles[off.x + r] = make_int4(t, 1, s, pl.nvis[t]);
+      continue;
+    }
     if (r % 8) continue;
     const int ntok = min(8, ql - r);
     const int nvmax = pl.nvis[t + ntok - 1];
-    const int2 off = pl.seq_tile_off[s];
     if (ntok == 1) pl.dec_tiles[off.x] = make_int4(t, ntok, s, nvmax);
     else pl.pre_tiles[off.y + r / 8] = make_int4(t, ntok, s, nvmax);
   }
@@ -512,13 +522,16 @@ int run_indexer(cudaStream_t stream, const IndexerMeta& m, const uint16_t* q, co
   int ch1 = kChunkDecode;
   const long long decode_keys = (long long)m.T * m.max_kv;
   while (ch1 < kChunkDecodeMax && 2 * ch1 <= 64 * m.ps && decode_keys / (2LL * ch1) >= 4LL * sms) ch1 *= 2;
-  DSA_LAUNCH_PDL(indexer_plan_kernel, dim3(1), dim3(1024), 0, stream, m, pl, ch1, kChunkPrefill);
+  // as many tokens as requests: a decode batch (or requests without new
+  // tokens beside multi-token ones, whose tokens are then scored one by one)
+  const int one_token = m.T == m.S ? 1 : 0;
+  DSA_LAUNCH_PDL(indexer_plan_kernel, dim3(1), dim3(1024), 0, stream, m, pl, ch1, kChunkPrefill, one_token);
   {
     using C = IdxCfg<1>;
     set_smem_attr_once(reinterpret_cast<const void*>(indexer_score_kernel<1>), C::SMEM);
     DSA_LAUNCH_PDL(indexer_score_kernel<1>, dim3(sms), dim3(C::THREADS), C::SMEM, stream, m, pl, out, kmap, qmap);
   }
-  {
+  if (!one_token) {
     using C = IdxCfg<8>;
     set_smem_attr_once(reinterpret_cast<const void*>(indexer_score_kernel<8>), C::SMEM);
     DSA_LAUNCH_PDL(indexer_score_kernel<8>, dim3(sms), dim3(C::THREADS), C::SMEM, stream, m, pl, out, kmap, qmap8);

@@ -17,6 +17,9 @@ CASES = {
     "extend": ([37], [500]),
     "mixed": ([1, 50, 0, 1, 9, 3], [700, 300, 40, 65, 1000, 4]),
     "tails": ([8, 17, 2], [8, 130, 129]),
+    # as many tokens as requests although two requests have several: the
+    # indexer plans every token as a one-token tile
+    "one_token": ([2, 0, 1, 3, 0, 0], [300, 40, 900, 129, 10, 64]),
 }
 
 
