@@ -135,32 +135,39 @@ class LayerRunner:
                   last_chunks=4):
         """One step from and to pinned host buffers (same shapes as the device
         tensors). The indexer inputs, the metadata and the new tokens' rows
-        are copied on the current stream; each layer's attention queries (the
-        largest inputs, needed only by that layer's attention) on the stream
+        are copied first, on the current stream: host-to-device copies of all
+        streams share one copy queue, so anything issued after the queries
+        would wait for them. Each layer's attention queries (the largest
+        inputs, needed only by that layer's attention) follow on the stream
         ``side``, in layer order, while the earlier layers compute; each
         layer's output is read back on the stream ``out_side`` (one of the
         runner's own if None) as soon as that layer's attention has written it,
         and the token selections of the first full slot once they exist. On a
-        prefill batch the last layer's attention runs in ``last_chunks`` token
-        ranges, each read back as soon as it is written, so little of the
-        final read-back is left after the last kernel. The current stream
-        joins both side streams before it returns, so the step ends when every
-        copy has landed. Can be captured in a CUDA graph."""
+        prefill batch the first layer's queries arrive, and its attention runs,
+        in ``last_chunks`` token ranges (the attention of the first range
+        starts when its queries have landed, not all of them), and the last
+        layer's attention runs in as many ranges, each read back as soon as it
+        is written, so little of the final read-back is left after the last
+        kernel. The current stream joins both side streams before it returns,
+        so the step ends when every copy has landed. Can be captured in a CUDA
+        graph."""
         cur = torch.cuda.current_stream(self.dev)
         if out_side is None:
             if getattr(self, "_out_side", None) is None:
                 self._out_side = torch.cuda.Stream(self.dev)
             out_side = self._out_side
-        # the previous step's kernels have finished reading q (its read-backs
-        # were joined into the current stream when it returned)
-        side.wait_stream(cur)
-        q_ready = []
-        with torch.cuda.stream(side):
-            for d, h in zip(self.q, h_q):
-                d.copy_(h, non_blocking=True)
-                ev = torch.cuda.Event()
-                ev.record(side)
-                q_ready.append(ev)
+        nl = len(self.types)
+
+        def ranges(layer):
+            # token ranges on query-block boundaries (first and last layer of a
+            # prefill batch), else the whole batch
+            nch = max(1, min(last_chunks, self.T // self.QB)) if (self.prefill and layer in (0, nl - 1)) else 1
+            if nch == 1:
+                return [(0, self.T)]
+            nqb = -(-self.T // self.QB)
+            b = [min(self.T, (nqb * c // nch) * self.QB) for c in range(nch)] + [self.T]
+            return list(zip(b[:-1], b[1:]))
+
         self.q_idx.copy_(h_q_idx, non_blocking=True)
         self.w.copy_(h_w, non_blocking=True)
         for d, h in zip(self.meta, h_meta):
@@ -169,8 +176,21 @@ class LayerRunner:
             d.copy_(h, non_blocking=True)
         for d, h in zip(self.new_k, h_new_k or []):
             d.copy_(h, non_blocking=True)
+        # the previous step's kernels have finished reading q (its read-backs
+        # were joined into the current stream when it returned)
+        side.wait_stream(cur)
+        q_ready = []  # per layer: one event per token range of its attention
+        with torch.cuda.stream(side):
+            for layer, (d, h) in enumerate(zip(self.q, h_q)):
+                evs = []
+                for b, e in ranges(layer) if layer == 0 else [(0, self.T)]:
+                    d[b:e].copy_(h[b:e], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(side)
+                    evs.append(ev)
+                q_ready.append(evs)
         topk_read = False
-        for layer in range(len(self.types)):
+        for layer in range(nl):
             self.write_back(layer)
             if self.full_slot[layer] >= 0:
                 slot = self.full_slot[layer]
@@ -182,15 +202,11 @@ class LayerRunner:
                     with torch.cuda.stream(out_side):
                         h_topk.copy_(self.topk[0], non_blocking=True)
                     topk_read = True
-            cur.wait_event(q_ready[layer])
-            last = layer == len(self.types) - 1
-            nch = max(1, min(last_chunks, self.T // self.QB)) if (self.prefill and last) else 1
-            bounds = [0, self.T]
-            if nch > 1:  # token ranges on query-block boundaries
-                nqb = -(-self.T // self.QB)
-                bounds = [min(self.T, (nqb * c // nch) * self.QB) for c in range(nch)] + [self.T]
-            for b, e in zip(bounds[:-1], bounds[1:]):
-                self.attend(layer, (b, e) if nch > 1 else None)
+            rs = ranges(layer)
+            for i, (b, e) in enumerate(rs):
+                evs = q_ready[layer]
+                cur.wait_event(evs[min(i, len(evs) - 1)])
+                self.attend(layer, (b, e) if len(rs) > 1 else None)
                 out_side.wait_stream(cur)
                 with torch.cuda.stream(out_side):
                     h_o[layer][b:e].copy_(self.o[layer][b:e], non_blocking=True)
