@@ -71,6 +71,19 @@ bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_bf16_3d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t groups,
+                    uint32_t box_rows) {
+  auto fn = get_encode();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {cols, rows, groups};
+  cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static bool ps_supported(int ps) { return ps == 32 || ps == 64 || ps == 128; }
 

@@ -363,7 +363,7 @@ __device__ __forceinline__ void mma_issuer(uint32_t tmem, uint32_t qs_addr, uint
 template <bool kSoftCap, int kCopyW>
 __global__ void __launch_bounds__((6 + kCopyW) * 32, 1)
     sparse_mla_kernel(const AttendParams prm, const __grid_constant__ CUtensorMap kvmap,
-                      const __grid_constant__ CUtensorMap qmap) {
+                      const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap) {
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {
     if (threadIdx.x == 0) set_status(prm.dev_status, DSA_STATUS_INTERNAL);
@@ -771,34 +771,46 @@ __global__ void __launch_bounds__((6 + kCopyW) * 32, 1)
         for (int j = 0; j < 32; ++j) oa[j] = ob[j] = 0u;
       }
     };
-    auto store_bf16_32 = [&](uint16_t* dst, const uint32_t (&ov)[32], float scale) {
-      uint32_t pk[16];
-#pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(ov[j]) * scale, __uint_as_float(ov[j + 1]) * scale);
-        pk[j >> 1] = *reinterpret_cast<uint32_t*>(&b2);
-      }
-      uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-      for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-    };
     auto store_bf16_4 = [&](uint16_t* dst, float4 a) {
       __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
       *reinterpret_cast<uint2*>(dst) = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
     };
     if (prm.nsplit == 1) {
-      // one split: each thread stores its own head row (measured faster here
-      // than the staged, line-wide stores of the split path below)
-      const size_t orow = ((size_t)t * prm.H + h) * kDv + half * kDvHalf;
+      // one split: the warp stages its 32 head rows as bf16 in the idle key
+      // stage (four 128-byte-swizzled boxes of 64 columns) and one lane
+      // writes them with four TMA stores; rows past H lie outside the tensor
+      // map and are not written. (Each thread storing its own row made every
+      // warp store touch 32 lines.)
+      uint8_t* stg = kst_s + (warp & 3) * 16384;
+      const uint32_t stg_a = smem_u32(stg);
 #pragma unroll 1
       for (int c0 = 0; c0 < kDvHalf; c0 += 64) {
         uint32_t oa[32], ob[32];
         load_o64(c0, oa, ob);
-        if (hv) {
-          store_bf16_32(prm.o + orow + c0, oa, inv_l);
-          store_bf16_32(prm.o + orow + c0 + 32, ob, inv_l);
+        const uint32_t box = stg_a + (uint32_t)(c0 / 64) * 4096u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t x0 = j < 4 ? oa[8 * j + 2 * e] : ob[8 * (j - 4) + 2 * e];
+            const uint32_t x1 = j < 4 ? oa[8 * j + 2 * e + 1] : ob[8 * (j - 4) + 2 * e + 1];
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(x0) * inv_l, __uint_as_float(x1) * inv_l);
+            pk[e] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          st_shared_v4(box + sw128_offset((uint32_t)lane, (uint32_t)j), pk[0], pk[1], pk[2], pk[3]);
         }
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+      const int hw = h0 + (warp & 3) * 32;  // first head row of this warp
+      if (lane == 0 && hw < prm.H) {
+#pragma unroll 1
+        for (int c = 0; c < kDvHalf / 64; ++c) tma_store_3d(&omap, stg + c * 4096, half * kDvHalf + c * 64, hw, t);
+        bulk_commit();
+        bulk_wait_read();
+      }
+      __syncwarp();
       if (hv && half == 0 && prm.lse) prm.lse[(size_t)t * prm.H + h] = lse_v;
     } else {
       // split keys: write this split's normalised partial; the last CTA of the
@@ -1001,8 +1013,10 @@ int run_attend(cudaStream_t stream, AttendParams prm, void* ws, size_t ws_bytes)
   if (!encode_bf16_2d(&kvmap, prm.kv, (uint64_t)prm.P * prm.ps, (uint64_t)prm.row_stride, 32, kDk))
     return DSA_ERR_CUDA;
   if (!encode_bf16_2d(&qmap, prm.q, (uint64_t)prm.T * prm.H, kDk, 128, kDk)) return DSA_ERR_CUDA;
+  CUtensorMap omap;  // the output [T][H][512] in boxes of 64 columns x 32 head rows
+  if (!encode_bf16_3d(&omap, prm.o, kDv, (uint64_t)prm.H, (uint64_t)prm.T, 32)) return DSA_ERR_CUDA;
   dim3 grid(cols, prm.tn > 0 ? prm.tn : prm.T, prm.nsplit);
-  void (*kern)(AttendParams, CUtensorMap, CUtensorMap);
+  void (*kern)(AttendParams, CUtensorMap, CUtensorMap, CUtensorMap);
   int threads;
   if (prm.soft_cap_on) {  // dense mode only: page runs
     kern = sparse_mla_kernel<true, kCopyWarpsRuns>;
@@ -1015,7 +1029,7 @@ int run_attend(cudaStream_t stream, AttendParams prm, void* ws, size_t ws_bytes)
     threads = (6 + kCopyWarpsRuns) * 32;
   }
   set_smem_attr_once(reinterpret_cast<const void*>(kern), kSmem);
-  DSA_LAUNCH_PDL(kern, grid, dim3(threads), kSmem, stream, prm, kvmap, qmap);
+  DSA_LAUNCH_PDL(kern, grid, dim3(threads), kSmem, stream, prm, kvmap, qmap, omap);
   return DSA_OK;
 }
 

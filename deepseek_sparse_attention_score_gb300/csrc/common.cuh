@@ -120,5 +120,9 @@ void set_smem_attr_once(const void* func, int bytes);
 // [64 cols x box_rows] box and 128-byte swizzle.
 bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_elems, uint32_t box_rows,
                     uint64_t used_cols);
+// [groups][rows][cols] bf16 (contiguous), boxes of 64 columns x box_rows rows
+// of one group, 128-byte swizzle
+bool encode_bf16_3d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t groups,
+                    uint32_t box_rows);
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 }  // namespace dsa
