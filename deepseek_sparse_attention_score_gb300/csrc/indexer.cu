@@ -7,7 +7,8 @@
 // NQ = 1 serves decode-like tiles (HBM-bound streaming of paged keys), NQ = 8
 // serves prefill tiles (tensor-bound). Keys arrive page by page through 2-D
 // TMA with 128-byte swizzle into a multi-stage ring; the epilogue writes the
-// fp32 token scores and/or the per-page max-pooled scores.
+// fp32 token scores and/or the maximum of every 32-key granule (the page top-k
+// folds a page's granules into its max-pooled score).
 //
 // A device-side planner turns the ragged metadata into work items
 // (query tile, key chunk) so the persistent kernels never read metadata the
