@@ -202,3 +202,33 @@ def test_page_topk_folds_visible_granules(dsa, full_pages):
                                      k_pages=k_pages, tokens=np.arange(1, T))
     prow = [O.page_scores_of_row(r, ps) for r in srows]
     check_topk_rows(got[1][1:], ref, k_pages, prow, what="page top-k")
+
+
+def test_long_context_chunked_prefill_rows(dsa):
+    """A chunk of new tokens at the end of a 600 K-token context: more rows
+    than twice the SM count, token rows of 600 K scores (read once with a
+    sampled threshold) and page rows of 9 K pages (longer than the short
+    blocks' stage: the wide blocks fold granules while staging). Sampled rows
+    are checked against the oracle."""
+    dev = torch.device("cuda")
+    n_new = 2 * dsa.dsa_device_sm_count() + 16
+    ctx = 600_000
+    ps, k, k_pages, seed = 64, 2048, 32, 85
+    rg = DI.make_ragged([n_new], [ctx], ps, master_seed=seed, spare_pages=1)
+    T = rg.T
+    q_idx = DI.randn((T, DI.INDEX_HEADS, DI.INDEX_DIM), seed, "q_idx").to(torch.bfloat16)
+    w = DI.rand((T, DI.INDEX_HEADS), seed, "w") / np.sqrt(DI.INDEX_HEADS)
+    kc = DI.randn((rg.num_pages, ps, DI.INDEX_DIM), seed, "kcache").to(torch.bfloat16)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    pages, topk = dsa.dsa_indexer_page_topk(q_idx.to(dev), w.to(dev), kc.to(dev), *meta_to(rg, dev),
+                                            k_pages=k_pages, max_kv=ctx, k=k, with_tokens=True, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    sample = np.array(sorted({0, 1, T // 3, T // 2, T - 2, T - 1}
+                             | set(np.random.default_rng(5).choice(T, 6, replace=False).tolist())))
+    kb = kc.view(torch.int16).numpy()
+    ref, srows = O.indexer_topk(f32(q_idx), f32(w), kb, **meta_np(rg), k=k, tokens=sample)
+    check_topk_rows(topk.cpu().numpy()[sample], ref, k, srows)
+    pref = O.topk_rows_of([O.page_scores_of_row(r, ps) for r in srows], k_pages)
+    prow = [O.page_scores_of_row(r, ps) for r in srows]
+    check_topk_rows(pages.cpu().numpy()[sample], pref, k_pages, prow, what="page top-k")
