@@ -145,8 +145,8 @@ def test_long_rows_sample_misleads(dsa):
     check_topk_rows(got, ref, wl.k, srows)
 
 
-@pytest.mark.parametrize("full_pages", [600, 34380])
-def test_page_topk_folds_visible_granules(dsa, full_pages):
+@pytest.mark.parametrize("ps,full_pages", [(64, 600), (64, 34380), (128, 600)])
+def test_page_topk_folds_visible_granules(dsa, ps, full_pages):
     """Page scores are folded from 32-key granule maxima. A page whose tail is
     not visible must ignore the granules past the visible length even when
     the workspace still holds larger values there from an earlier call with a
@@ -155,7 +155,7 @@ def test_page_topk_folds_visible_granules(dsa, full_pages):
     Keys are zero except planted copies of two vectors A and B = A / 2, so
     the expected selection follows from the oracle's scores of A and B."""
     dev = torch.device("cuda")
-    ps, k_pages, seed = 64, 16, 83
+    k_pages, seed = 16, 83
     n_long, n_short = full_pages * ps + 60, full_pages * ps + 20  # same page count
     q_lens = [1, 1, 1, 1]
     rgs = [DI.make_ragged(q_lens, [n, 1000, 1500, 700], ps, master_seed=seed, spare_pages=2)
