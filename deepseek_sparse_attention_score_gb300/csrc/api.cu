@@ -115,7 +115,7 @@ static int indexer_common(cudaStream_t stream, const uint16_t* q, const float* w
   if (T >= (1 << 24) || S >= (1 << 24)) return DSA_ERR_UNSUPPORTED;
   const IndexerLayout L = indexer_layout(T, S, max_kv, ps);
   if (!ws || ws_bytes < L.total || !aligned16(ws)) return DSA_ERR_WORKSPACE;
-  IndexerMeta m{w, seq_lens, cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps, max_kv, dev_status};
+  IndexerMeta m{w, seq_lens, cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps, max_kv, dev_status, 0, 0};
   IndexerPlan pl;
   IndexerOut out;
   rc = run_indexer(stream, m, q, kcache, ws, L, topk != nullptr, topk_pages != nullptr, &pl, &out);
@@ -255,7 +255,7 @@ int dsa_indexer_topk_approx(dsa_stream_t stream, const uint16_t* q, const float*
   if (T >= (1 << 24) || S >= (1 << 24)) return DSA_ERR_UNSUPPORTED;
   const IndexerLayout L = indexer_layout(T, S, max_kv, ps);
   if (!ws || ws_bytes < L.total + approx_extra(T, k, over, max_kv) || !aligned16(ws)) return DSA_ERR_WORKSPACE;
-  IndexerMeta m{w, seq_lens, cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps, max_kv, dev_status};
+  IndexerMeta m{w, seq_lens, cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps, max_kv, dev_status, 0, 0};
   IndexerPlan pl;
   IndexerOut out;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -173,6 +173,28 @@ __global__ void __launch_bounds__(1024) indexer_plan_kernel(IndexerMeta m, Index
 }
 
 // ------------------------------------------------------------------ scorer
+// Item ii of a launch without a planner (every request has one new token, so
+// token t is request t unless some requests have none): token, request, key
+// range and the token's visible length, clamped to its page-table span as
+// the planner clamps it. Returns false for an empty key range.
+__device__ __forceinline__ bool direct_item(const IndexerMeta& m, int ii, int& t, int& seq, int& kb, int& ke,
+                                            int& nv) {
+  t = ii / m.direct_nch;
+  const int c = ii - t * m.direct_nch;
+  const int a = __ldg(m.cu_q_lens + t), b = __ldg(m.cu_q_lens + t + 1);
+  seq = (a == t && b == t + 1) ? t : seq_of_token(m.cu_q_lens, m.S, t);
+  const TokenGeom g = token_geom(m.seq_lens, m.cu_q_lens, m.cu_kv_lens, m.S, m.ps, m.max_kv, t, m.dev_status, seq);
+  const long long cap = (long long)(m.PTW - g.page_base) * m.ps;
+  nv = g.n_vis;
+  if (g.page_base < 0 || (long long)nv > cap) {
+    set_status(m.dev_status, DSA_STATUS_BAD_METADATA);
+    nv = cap < 0 || g.page_base < 0 ? 0 : (int)cap;
+  }
+  kb = c * m.direct_ch;
+  ke = min(nv, kb + m.direct_ch);
+  return kb < ke;
+}
+
 template <int NQ>
 struct IdxCfg {
   static constexpr int N = NQ * 32;                  // UMMA N: (query, head) columns
@@ -211,7 +233,8 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::THREADS, 1)
   extern __shared__ __align__(1024) uint8_t smem[];
   griddep_launch_dependents();
   griddep_wait();
-  const int n_items = NQ == 1 ? pl.counts[0] : pl.counts[1];
+  const bool direct = NQ == 1 && m.direct_nch > 0;
+  const int n_items = direct ? m.T * m.direct_nch : NQ == 1 ? pl.counts[0] : pl.counts[1];
   if ((int)blockIdx.x >= n_items) return;
   const int4* items = NQ == 1 ? pl.dec_items : pl.pre_items;
   if (smem_u32(smem) & 1023u) {  // the swizzled layouts need 1 KB alignment
@@ -269,9 +292,24 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::THREADS, 1)
     }
     int kt = 0, it = 0;
     bool ok = true;
+    if (direct && blockIdx.x == 0 && lane == 0 &&
+        (__ldg(m.cu_q_lens) != 0 || __ldg(m.cu_q_lens + m.S) != m.T))
+      set_status(m.dev_status, DSA_STATUS_BAD_METADATA);
     for (int ii = blockIdx.x; ii < n_items && ok; ii += gridDim.x, ++it) {
-      const int4 item = items[ii];
-      const int t0 = item.x, ntok = item.y >> 24, seq = item.y & 0xFFFFFF, kb = item.z, ke = item.w;
+      int t0, ntok, seq, kb, ke;
+      if (direct) {
+        int nvv;
+        const bool live = direct_item(m, ii, t0, seq, kb, ke, nvv);
+        if (lane == 0 && kb == 0) pl.nvis[t0] = nvv;  // the token's first item
+        if (!live) {  // every role skips the same items
+          --it;
+          continue;
+        }
+        ntok = 1;
+      } else {
+        const int4 item = items[ii];
+        t0 = item.x, ntok = item.y >> 24, seq = item.y & 0xFFFFFF, kb = item.z, ke = item.w;
+      }
       const int qb = it & 1;
       int okl = 1;
       if (lane == 0) {
@@ -345,8 +383,17 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::THREADS, 1)
       int kt = 0, dt = 0, it = 0;
       bool ok = true;
       for (int ii = blockIdx.x; ii < n_items && ok; ii += gridDim.x, ++it) {
-        const int4 item = items[ii];
-        const int kb = item.z, ke = item.w;
+        int kb, ke;
+        if (direct) {
+          int t_, s_, nv_;
+          if (!direct_item(m, ii, t_, s_, kb, ke, nv_)) {
+            --it;
+            continue;
+          }
+        } else {
+          const int4 item = items[ii];
+          kb = item.z, ke = item.w;
+        }
         const int qb = it & 1;
         if (!(ok = mbar_wait(qfull + qb, (it >> 1) & 1, abort_flag))) break;
         const uint32_t qaddr = smem_u32(q_s + qb * C::Q_BYTES);
@@ -387,15 +434,27 @@ __global__ void __launch_bounds__(IdxCfg<NQ>::THREADS, 1)
     int dt = 0, it = 0;
     bool ok = true;
     for (int ii = blockIdx.x; ii < n_items && ok; ii += gridDim.x, ++it) {
-      const int4 item = items[ii];
-      const int t0 = item.x, ntok = item.y >> 24, kb = item.z, ke = item.w;
-      const int qb = it & 1;
+      int t0, ntok, kb, ke;
       int nv[QPW];
+      if (direct) {
+        int s_, nv_;
+        if (!direct_item(m, ii, t0, s_, kb, ke, nv_)) {
+          --it;
+          continue;
+        }
+        ntok = 1;
 #pragma unroll
-      for (int j = 0; j < QPW; ++j) {
-        const int q = qset * QPW + j;
-        nv[j] = q < ntok ? pl.nvis[t0 + q] : 0;
+        for (int j = 0; j < QPW; ++j) nv[j] = qset * QPW + j < ntok ? nv_ : 0;
+      } else {
+        const int4 item = items[ii];
+        t0 = item.x, ntok = item.y >> 24, kb = item.z, ke = item.w;
+#pragma unroll
+        for (int j = 0; j < QPW; ++j) {
+          const int q = qset * QPW + j;
+          nv[j] = q < ntok ? pl.nvis[t0 + q] : 0;
+        }
       }
+      const int qb = it & 1;
       if (!(ok = mbar_wait(qfull + qb, (it >> 1) & 1, abort_flag))) break;
       const float* wq = w_s + qb * C::N;
       for (int tile = kb / 128; tile * 128 < ke; ++tile, ++dt) {
@@ -526,11 +585,18 @@ int run_indexer(cudaStream_t stream, const IndexerMeta& m, const uint16_t* q, co
   // as many tokens as requests: a decode batch (or requests without new
   // tokens beside multi-token ones, whose tokens are then scored one by one)
   const int one_token = m.T == m.S ? 1 : 0;
-  DSA_LAUNCH_PDL(indexer_plan_kernel, dim3(1), dim3(1024), 0, stream, m, pl, ch1, kChunkPrefill, one_token);
+  IndexerMeta m1 = m;
+  if (one_token) {
+    // no planner: the one-query kernel derives its items from the token index
+    m1.direct_nch = (int)((m.max_kv + ch1 - 1) / ch1);
+    m1.direct_ch = ch1;
+  } else {
+    DSA_LAUNCH_PDL(indexer_plan_kernel, dim3(1), dim3(1024), 0, stream, m, pl, ch1, kChunkPrefill, one_token);
+  }
   {
     using C = IdxCfg<1>;
     set_smem_attr_once(reinterpret_cast<const void*>(indexer_score_kernel<1>), C::SMEM);
-    DSA_LAUNCH_PDL(indexer_score_kernel<1>, dim3(sms), dim3(C::THREADS), C::SMEM, stream, m, pl, out, kmap, qmap);
+    DSA_LAUNCH_PDL(indexer_score_kernel<1>, dim3(sms), dim3(C::THREADS), C::SMEM, stream, m1, pl, out, kmap, qmap);
   }
   if (!one_token) {
     using C = IdxCfg<8>;

@@ -18,6 +18,9 @@ struct IndexerMeta {
   const int32_t* page_indices;
   int T, S, P, PTW, ps, max_kv;
   int32_t* dev_status;
+  // one-token launches without a planner: item ii is token ii / direct_nch,
+  // keys [c, c + 1) * direct_ch of it with c = ii % direct_nch (0: planned)
+  int direct_nch, direct_ch;
 };
 
 struct IndexerPlan {
