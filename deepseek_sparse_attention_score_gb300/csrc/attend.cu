@@ -36,11 +36,12 @@ namespace dsa {
 namespace {
 // warp 0 MMA, warp 1 key generator, warps 2-3 and 8.. gather, warps 4-7 softmax.
 // Scattered token rows are copied by ten warps (512 threads: more copies in
-// flight, measured 10% faster decode than six); the page-run modes, whose
-// steps are single TMA boxes, run with six (384 threads) in an instantiation
-// of their own.
+// flight, measured 10% faster decode than six, as fast as eight); the
+// page-run modes, whose steps are single TMA boxes, run with four (320
+// threads) in an instantiation of their own (measured against 2, 3, 5, 6 and
+// 8: query-block prefill 6.50 ms with six, 6.35 with four).
 constexpr int kCopyWarpsToken = 10;
-constexpr int kCopyWarpsRuns = 6;
+constexpr int kCopyWarpsRuns = 4;
 constexpr int kSubKeys = 32;   // keys resolved / copied per generator step
 constexpr int kTileKeys = 64;  // keys per MMA tile (two generator steps)
 constexpr int kRing = 12;      // generator steps buffered ahead of the gather
