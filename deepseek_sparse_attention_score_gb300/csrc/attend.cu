@@ -44,7 +44,7 @@ constexpr int kCopyWarpsToken = 10;
 constexpr int kCopyWarpsRuns = 4;
 constexpr int kSubKeys = 32;   // keys resolved / copied per generator step
 constexpr int kTileKeys = 64;  // keys per MMA tile (two generator steps)
-constexpr int kRing = 12;      // generator steps buffered ahead of the gather
+constexpr int kRing = 18;      // generator steps buffered ahead of the gather
 constexpr int kDk = 576, kDv = 512, kDvHalf = 256;
 constexpr int kBlk = kTileKeys * 128;   // one 64-dim column block of a tile: 8 KB
 constexpr int kKBlocks = 5, kVBlocks = 4;
