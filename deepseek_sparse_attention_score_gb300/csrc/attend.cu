@@ -44,7 +44,11 @@ constexpr int kCopyWarpsToken = 10;
 constexpr int kCopyWarpsRuns = 4;
 constexpr int kSubKeys = 32;   // keys resolved / copied per generator step
 constexpr int kTileKeys = 64;  // keys per MMA tile (two generator steps)
-constexpr int kRing = 18;      // generator steps buffered ahead of the gather
+// generator steps buffered ahead of the gather: token mode keeps 32 physical
+// rows per step, the page-run modes only a step's first row, so their ring
+// can be deeper in the same shared memory
+constexpr int kRingToken = 18;
+constexpr int kRingRuns = 32;
 constexpr int kDk = 576, kDv = 512, kDvHalf = 256;
 constexpr int kBlk = kTileKeys * 128;   // one 64-dim column block of a tile: 8 KB
 constexpr int kKBlocks = 5, kVBlocks = 4;
@@ -57,15 +61,23 @@ constexpr int kQsBytes = (kDk - kQTmemDims) / 64 * 16384;  // 5 column blocks x 
 constexpr int OFF_QS = 0;
 constexpr int OFF_KST = OFF_QS + kQsBytes;
 constexpr int OFF_VST = OFF_KST + kKStages * kKStageBytes;
-constexpr int OFF_RING = OFF_VST + kVStages * kVStageBytes;  // int32 [kRing][32] physical rows
-constexpr int OFF_RINFO = OFF_RING + kRing * 32 * 4;         // uint32 mask[kRing], end[kRing]
-constexpr int OFF_RBASE = OFF_RINFO + kRing * 8;             // int32 base row of contiguous steps [kRing]
-constexpr int OFF_SINFO = OFF_RBASE + kRing * 4;  // uint32 kend[kKStages], vmask[kVStages][2], vend[kVStages]
-constexpr int OFF_BAR = (OFF_SINFO + (kKStages + 3 * kVStages) * 4 + 7) & ~7;
-constexpr int NBAR = 2 * kKStages + 2 * kVStages + 2 * kRing + 7;
-constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-constexpr int kSmem = OFF_MISC + 16;
-static_assert(kSmem <= 227 * 1024, "shared memory budget");
+// the tail of the shared-memory layout, after the value stages: the
+// generator ring (R steps; ROWS: with 32 physical rows per step), stage
+// flags, barriers and a few words
+template <int R, bool ROWS>
+struct RingLayout {
+  static constexpr int OFF_RING = OFF_VST + kVStages * kVStageBytes;  // int32 [R][32] physical rows (ROWS)
+  static constexpr int OFF_RINFO = OFF_RING + (ROWS ? R * 32 * 4 : 0);  // uint32 mask[R], end[R]
+  static constexpr int OFF_RBASE = OFF_RINFO + R * 8;   // int32 first row of each step [R]
+  static constexpr int OFF_SINFO = OFF_RBASE + R * 4;   // uint32 kend[kKStages], vmask[kVStages][2], vend[kVStages]
+  static constexpr int OFF_BAR = (OFF_SINFO + (kKStages + 3 * kVStages) * 4 + 7) & ~7;
+  static constexpr int NBAR = 2 * kKStages + 2 * kVStages + 2 * R + 7;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 16;
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
+template <int kCopyW>
+using LayoutOf = RingLayout<kCopyW == kCopyWarpsToken ? kRingToken : kRingRuns, kCopyW == kCopyWarpsToken>;
 static_assert(OFF_KST % 1024 == 0 && OFF_VST % 1024 == 0, "swizzle atoms need 1 KB alignment");
 constexpr uint32_t kIdescQK = make_idesc_bf16(128, kTileKeys, false, false);
 constexpr uint32_t kIdescPV = make_idesc_bf16(128, kDvHalf, false, true);
@@ -380,14 +392,17 @@ __global__ void __launch_bounds__((6 + kCopyW) * 32, 1)
   uint8_t* qs_s = smem + OFF_QS;
   uint8_t* kst_s = smem + OFF_KST;
   uint8_t* vst_s = smem + OFF_VST;
-  int* ring_rows = reinterpret_cast<int*>(smem + OFF_RING);
-  volatile uint32_t* ring_mask = reinterpret_cast<volatile uint32_t*>(smem + OFF_RINFO);
+  using L = LayoutOf<kCopyW>;
+  constexpr int kRing = kCopyW == kCopyWarpsToken ? kRingToken : kRingRuns;
+  constexpr bool kRows = kCopyW == kCopyWarpsToken;  // page-run steps carry only their first row
+  int* ring_rows = reinterpret_cast<int*>(smem + L::OFF_RING);
+  volatile uint32_t* ring_mask = reinterpret_cast<volatile uint32_t*>(smem + L::OFF_RINFO);
   volatile uint32_t* ring_end = ring_mask + kRing;
-  volatile int* ring_base = reinterpret_cast<volatile int*>(smem + OFF_RBASE);
-  volatile uint32_t* kst_end = reinterpret_cast<volatile uint32_t*>(smem + OFF_SINFO);
+  volatile int* ring_base = reinterpret_cast<volatile int*>(smem + L::OFF_RBASE);
+  volatile uint32_t* kst_end = reinterpret_cast<volatile uint32_t*>(smem + L::OFF_SINFO);
   volatile uint32_t* vst_mask = kst_end + kKStages;   // [kVStages][2]
   volatile uint32_t* vst_end = vst_mask + 2 * kVStages;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* kfull = bars;                 // [kKStages] full_arrivals + tx bytes
   uint64_t* kempty = kfull + kKStages;    // [kKStages] commit after the K-part MMAs
   uint64_t* vfull = kempty + kKStages;    // [kVStages] full_arrivals + tx bytes
@@ -399,8 +414,8 @@ __global__ void __launch_bounds__((6 + kCopyW) * 32, 1)
   uint64_t* pempty = sfull + 4;           // PV commit
   uint64_t* fin = sfull + 5;
   uint64_t* qbar = sfull + 6;             // the query block's TMA copy
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
 
   if (tid == 0) {
     for (int i = 0; i < kKStages; ++i) {
@@ -511,7 +526,7 @@ __global__ void __launch_bounds__((6 + kCopyW) * 32, 1)
       if (lane == 0) ok = mbar_wait(rempty + slot, ((j / kRing) & 1) ^ 1, abort_flag) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) return false;
-      ring_rows[slot * 32 + lane] = end ? -1 : (int)row;
+      if constexpr (kRows) ring_rows[slot * 32 + lane] = end ? -1 : (int)row;
       if (lane == 0) {
         ring_mask[slot] = end ? 0u : mask;
         ring_end[slot] = end ? 1u : 0u;
@@ -590,8 +605,10 @@ __global__ void __launch_bounds__((6 + kCopyW) * 32, 1)
       for (int sb = 0; sb < 2; ++sb) {
         const int slot = sb ? s1 : s0, cbase = sb ? base1 : base0;
         const uint32_t d = kd + sb * (kSubKeys * 128);
-        if (cbase >= 0) {
-          // 32 consecutive rows of one page: one 2-D TMA box (64 cols x 32 rows) per block
+        // page-run modes: every step is 32 consecutive rows of one page, one
+        // 2-D TMA box (64 cols x 32 rows) per block; token mode: every step
+        // is 32 scattered rows
+        if constexpr (!kRows) {
           if (ctid == 0) {
             mbar_arrive_expect_tx(kfull + ks, kKBlocks * kSubKeys * 128);
 #pragma unroll 1
@@ -627,7 +644,7 @@ __global__ void __launch_bounds__((6 + kCopyW) * 32, 1)
       for (int sb = 0; sb < 2; ++sb) {
         const int slot = sb ? s1 : s0, cbase = sb ? base1 : base0;
         const uint32_t d = vd + sb * (kSubKeys * 128);
-        if (cbase >= 0) {
+        if constexpr (!kRows) {
           if (ctid == 0) {
             mbar_arrive_expect_tx(vfull + vs, kVBlocks * kSubKeys * 128);
 #pragma unroll 1
@@ -1018,19 +1035,22 @@ int run_attend(cudaStream_t stream, AttendParams prm, void* ws, size_t ws_bytes)
   if (!encode_bf16_3d(&omap, prm.o, kDv, (uint64_t)prm.H, (uint64_t)prm.T, 32)) return DSA_ERR_CUDA;
   dim3 grid(cols, prm.tn > 0 ? prm.tn : prm.T, prm.nsplit);
   void (*kern)(AttendParams, CUtensorMap, CUtensorMap, CUtensorMap);
-  int threads;
+  int threads, smem_bytes;
   if (prm.soft_cap_on) {  // dense mode only: page runs
     kern = sparse_mla_kernel<true, kCopyWarpsRuns>;
     threads = (6 + kCopyWarpsRuns) * 32;
+    smem_bytes = LayoutOf<kCopyWarpsRuns>::SMEM;
   } else if (prm.mode == kModeToken) {
     kern = sparse_mla_kernel<false, kCopyWarpsToken>;
     threads = (6 + kCopyWarpsToken) * 32;
+    smem_bytes = LayoutOf<kCopyWarpsToken>::SMEM;
   } else {
     kern = sparse_mla_kernel<false, kCopyWarpsRuns>;
     threads = (6 + kCopyWarpsRuns) * 32;
+    smem_bytes = LayoutOf<kCopyWarpsRuns>::SMEM;
   }
-  set_smem_attr_once(reinterpret_cast<const void*>(kern), kSmem);
-  DSA_LAUNCH_PDL(kern, grid, dim3(threads), kSmem, stream, prm, kvmap, qmap, omap);
+  set_smem_attr_once(reinterpret_cast<const void*>(kern), smem_bytes);
+  DSA_LAUNCH_PDL(kern, grid, dim3(threads), smem_bytes, stream, prm, kvmap, qmap, omap);
   return DSA_OK;
 }
 
