@@ -906,13 +906,11 @@ __global__ void __launch_bounds__((6 + kCopyW) * 32, 1)
         if (hv && half == 0 && prm.lse) prm.lse[(size_t)t * prm.H + h] = tot > 0.f ? mx + logf(tot) : -INFINITY;
         __syncwarp();
         // the warp merges its 32 rows, four at a time; this CTA's own split
-        // is read from the stage, the others from the partials. Token mode
-        // adds the splits in the fixed order 0, 1, ..., so a decode output does
-        // not depend on which CTA merges; the page-run instantiation starts
-        // from its own split (adding the fixed order there cost the query-block
-        // prefill 2% and the dense prefill 3% through code layout alone,
-        // although the query-block path never splits)
-        constexpr bool kFixedOrder = kCopyW == kCopyWarpsToken;
+        // is read from the stage, the others from the partials. The splits
+        // are added in the fixed order 0, 1, ..., so a decode output does not
+        // depend on which CTA of its row merges (measured: no cost in the
+        // page-run instantiation since its copier and ring changed; it had
+        // cost 2-3% through code layout before)
         const int rw = (warp & 3) * 32;  // first row of this warp
         const float* parts = prm.o_part + orow0;
         const size_t zstride = (size_t)prm.T * prm.H * kDv;
@@ -921,23 +919,13 @@ __global__ void __launch_bounds__((6 + kCopyW) * 32, 1)
           float4 acc[4][2];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            if constexpr (kFixedOrder) {
-              acc[u][0] = make_float4(0.f, 0.f, 0.f, 0.f);
-              acc[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-            } else {
-              const float w = wts[split * 128 + rw + i0 + u];
-              const float* sr = stg + (i0 + u) * kStageLd;
-              const float4 a = *reinterpret_cast<const float4*>(sr + 4 * lane);
-              const float4 b = *reinterpret_cast<const float4*>(sr + 128 + 4 * lane);
-              acc[u][0] = make_float4(a.x * w, a.y * w, a.z * w, a.w * w);
-              acc[u][1] = make_float4(b.x * w, b.y * w, b.z * w, b.w * w);
-            }
+            acc[u][0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            acc[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
           }
 #pragma unroll 1
           for (int z = 0; z < prm.nsplit; ++z) {
-            if (!kFixedOrder && z == split) continue;
             float4 va[4][2];
-            if (kFixedOrder && z == split) {
+            if (z == split) {
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
                 const float* sr = stg + (i0 + u) * kStageLd;

@@ -173,12 +173,9 @@ DSA_API int dsa_build_block_union(dsa_stream_t stream, const int32_t* topk_units
  *          (split-key partials; 0 bytes needed when T*H is large)
  * Supported: Dk == 576, Dv == 512, row_stride in {576, 640}, ps in
  * {32, 64, 128}, H >= 1 (heads are processed 128 at a time).
- * Reproducibility: with token units (unit == 1) every output is the same
- * on every run: when a row's keys are split across CTAs (few queries, long
- * selections) the splits are added in a fixed order. With page units a
- * split row is merged by whichever CTA of the row finishes last, starting
- * from its own split, so o may differ between runs by one bf16 rounding;
- * lse and every single-split row are the same on every run.
+ * Reproducibility: every output is the same on every run: when a row's
+ * keys are split across CTAs (few queries, long selections) the merging CTA
+ * adds the splits in a fixed order, whichever CTA of the row finishes last.
  * ------------------------------------------------------------------------ */
 DSA_API size_t dsa_sparse_mla_decode_workspace_size(int T, int H, int Dv);
 DSA_API int dsa_sparse_mla_decode(dsa_stream_t stream, const uint16_t* q, const uint16_t* kv, int row_stride,

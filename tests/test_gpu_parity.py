@@ -153,25 +153,26 @@ def test_sparse_mla_decode_most_splits(dsa, unit_kind, H):
     np.testing.assert_allclose(l[fin], ref_l[fin], rtol=1e-4, atol=1e-4)
 
 
-def test_sparse_mla_decode_token_splits_reproducible(dsa):
-    """Token-mode decode rows split over several CTAs merge their splits in a
-    fixed order: repeated calls give the same output bits, whichever CTA of
-    a row finishes last."""
+@pytest.mark.parametrize("unit,K", [(1, 1024), (64, 40)])
+def test_sparse_mla_decode_splits_reproducible(dsa, unit, K):
+    """Decode rows split over several CTAs (token and page units) merge their
+    splits in a fixed order: repeated calls give the same output bits,
+    whichever CTA of a row finishes last."""
     dev = torch.device("cuda")
     wl = DI.random_small(419, [1, 1, 1], [4000, 3000, 2500], H=128, k=64)
     rg = wl.rg
-    sel = _rand_sel(np.random.default_rng(12), rg, 1024, 1, dense=True)
+    sel = _rand_sel(np.random.default_rng(12), rg, K, unit, dense=True)
     meta = meta_to(rg, dev)
     q, kv, s = wl.q[0].to(dev), wl.kv[0].to(dev), torch.from_numpy(sel).to(dev)
     assert dsa.dsa_sparse_mla_decode_workspace_size(rg.T, 128) > 0, "the rows must be split"
     outs = []
     for _ in range(6):
-        o = dsa.dsa_sparse_mla_decode(q, kv, *meta, s, unit=1, sm_scale=wl.sm_scale)
+        o = dsa.dsa_sparse_mla_decode(q, kv, *meta, s, unit=unit, sm_scale=wl.sm_scale)
         torch.cuda.synchronize()
         outs.append(o.view(torch.int16).cpu().numpy())
     for o in outs[1:]:
         assert np.array_equal(o, outs[0]), "split decode output changed between identical calls"
-    ref_o, _ = O.sparse_mla(f32(wl.q[0]), f32(wl.kv[0]), **meta_np(rg), sel=sel, unit=1, sm_scale=wl.sm_scale,
+    ref_o, _ = O.sparse_mla(f32(wl.q[0]), f32(wl.kv[0]), **meta_np(rg), sel=sel, unit=unit, sm_scale=wl.sm_scale,
                             Dv=512)
     check_attention(torch.from_numpy(outs[0]).view(torch.bfloat16), ref_o)
 
