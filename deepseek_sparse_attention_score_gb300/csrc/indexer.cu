@@ -586,9 +586,10 @@ int run_indexer(cudaStream_t stream, const IndexerMeta& m, const uint16_t* q, co
   // tokens beside multi-token ones, whose tokens are then scored one by one)
   const int one_token = m.T == m.S ? 1 : 0;
   IndexerMeta m1 = m;
-  if (one_token) {
+  const long long nch = (m.max_kv + ch1 - 1) / ch1;
+  if (one_token && (long long)m.T * nch < (1LL << 31)) {
     // no planner: the one-query kernel derives its items from the token index
-    m1.direct_nch = (int)((m.max_kv + ch1 - 1) / ch1);
+    m1.direct_nch = (int)nch;
     m1.direct_ch = ch1;
   } else {
     DSA_LAUNCH_PDL(indexer_plan_kernel, dim3(1), dim3(1024), 0, stream, m, pl, ch1, kChunkPrefill, one_token);
