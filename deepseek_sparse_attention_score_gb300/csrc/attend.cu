@@ -23,9 +23,11 @@
 // them; the other five (the "K part") as soon as QK^T has.
 //
 // Keys are resolved 32 at a time by one warp (token top-k rows, page top-k
-// rows, or a query block's union + membership bitmap); runs of 32
-// consecutive rows of one page are fetched with 2-D TMA boxes, scattered
-// rows with coalesced cp.async. Masked keys are zero-filled or carry P = 0.
+// rows, or a query block's union + membership bitmap). The page-run modes
+// (page units, query blocks, dense) fetch every step, 32 consecutive rows of
+// one page, with 2-D TMA boxes; token mode fetches its scattered rows with
+// coalesced cp.async; each has an instantiation of its own. Masked keys are
+// zero-filled or carry P = 0.
 #include <atomic>
 
 #include "common.cuh"

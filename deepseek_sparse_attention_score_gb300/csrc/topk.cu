@@ -548,9 +548,10 @@ __device__ bool select_row_two_pass(const float* __restrict__ g, int n, int k, i
 
 // Row longer than shared memory, in one read: a threshold t0 from a strided
 // sample of the row bounds the candidates.
-//  A. kSample keys at evenly spaced positions; t0 = the sample's key of rank
-//     r, r chosen so that about (k + capacity) / 2 keys of the row are
-//     expected at or above t0 (halfway between too few and too many);
+//  A. kSample keys at evenly spaced positions; r is chosen so that about
+//     min(2k, (k + capacity) / 2) keys of the row are expected at or above
+//     the sample's key of rank r, and t0 is the lower bound of that key's
+//     16-bit bin (so a little below it);
 //  B. one pass over the row in block-wide chunks copies every key >= t0,
 //     in position order, into the candidate list (per chunk, each warp takes
 //     a contiguous run; a scan over the warps gives the offsets);
