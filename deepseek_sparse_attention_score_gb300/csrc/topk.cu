@@ -18,8 +18,7 @@
 namespace dsa {
 
 constexpr int kTopkThreads = 512;
-constexpr int kTopkThreadsShort = 128;  // threads per row when every row has at most kTopkShortCap keys
-constexpr int kTopkShortCap = 8192;
+constexpr int kTopkThreadsShort = 128;  // threads per row when every row has at most 2048 keys
 constexpr int kTopkThreadsMany = 256;   // threads per row for many rows of any length
 
 // Order-preserving map fp32 -> uint32 (larger float -> larger key); -0 and +0
@@ -701,10 +700,9 @@ __device__ void select_row_staged(const float* __restrict__ g, const uint32_t* _
   emit_ordered<true, TPB>(g, s_row, n, prefix, remaining, out_idx, out_val, s_tmp);
 }
 
-// TPB threads per row: kTopkThreads (a few rows of any length: the shortest
-// per-row time), kTopkThreadsMany (many rows, some long: three rows resident
-// per SM instead of one) or kTopkThreadsShort (many rows that all fit a
-// stage of kTopkShortCap keys)
+// TPB threads per row: kTopkThreads (a few rows longer than 2048: the
+// shortest per-row time), kTopkThreadsMany (many such rows: three resident
+// per SM instead of one) or kTopkThreadsShort (rows of at most 2048 keys)
 template <int TPB>
 __global__ void __launch_bounds__(TPB, TPB == kTopkThreadsMany ? 3 : 1)
     topk_rows_kernel(const float* __restrict__ scores, long long ld, const int* __restrict__ nvis, int div, int k,
@@ -763,14 +761,15 @@ __global__ void __launch_bounds__(TPB, TPB == kTopkThreadsMany ? 3 : 1)
   // (the short-row instantiation is only launched when every row fits cap)
 }
 
-// The block size for a launch: short blocks pay off when their extra rows
-// per SM are there to fill it (many rows) or the rows are short; a few long
-// rows keep the wide block (measured: 32 rows of 4-8 K keys took 61 us with
-// short blocks, 41 us wide).
+// The block size for a launch: rows of at most 2048 keys take 128-thread
+// blocks (six rows per SM, cheap block barriers); launches with many longer
+// rows take 256-thread blocks (three rows per SM); a few longer rows keep
+// the 512-thread block, the shortest time per row (measured: 32 rows of 4-8 K
+// keys took 61 us with short blocks, 41 us wide; 8192 causal rows of up to
+// 8192 keys 0.545 ms with short blocks, 0.530 with 256-thread ones).
 static int topk_tier(int T, int max_len) {
-  const bool many = T >= 2 * sm_count();
-  if (max_len <= kTopkShortCap && (many || max_len <= 2048)) return kTopkThreadsShort;
-  return many ? kTopkThreadsMany : kTopkThreads;
+  if (max_len <= 2048) return kTopkThreadsShort;
+  return T >= 2 * sm_count() ? kTopkThreadsMany : kTopkThreads;
 }
 
 static int topk_stage_cap(int tpb) {
