@@ -16,6 +16,7 @@ from .abi import (  # noqa: F401
     dsa_sparse_mla_decode,
     dsa_sparse_mla_decode_noalloc,
     dsa_paged_write_back,
+    dsa_paged_write_back_pair,
     dsa_dense_mla,
     dsa_selftest_wait_timeout,
     dsa_indexer_topk_approx,

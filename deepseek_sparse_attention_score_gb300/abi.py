@@ -43,6 +43,7 @@ EXPORTS = (
     "dsa_sparse_mla_prefill_qblock",
     "dsa_sparse_mla_prefill_qblock_range",
     "dsa_paged_write_back",
+    "dsa_paged_write_back_pair",
     "dsa_dense_mla",
     "dsa_selftest_wait_timeout",
     "dsa_indexer_topk_approx_workspace_size",
@@ -96,6 +97,8 @@ def lib() -> ctypes.CDLL:
     L.dsa_sparse_mla_decode_noalloc.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                                 _I, _I, _F, _P, _P, _P]
     L.dsa_paged_write_back.argtypes = [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]
+    L.dsa_paged_write_back_pair.argtypes = [_P, _P, _I, _I, _P, _I, _P, _I, _I, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I,
+                                            _I, _P]
     L.dsa_topk_pages_from_tokens.argtypes = [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P]
     L.dsa_dense_mla.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _F,
                                 _P, _P, _P, _Z, _P]
@@ -376,6 +379,32 @@ def dsa_paged_write_back(rows, cache, seq_lens, cu_q_lens, cu_kv_lens, page_indi
                                     PTW, ps, _ptr(dev_status))
     _check("dsa_paged_write_back", rc)
     return cache
+
+
+def dsa_paged_write_back_pair(rows0, cache0, rows1, cache1, seq_lens, cu_q_lens, cu_kv_lens, page_indices, *,
+                              D0=None, D1=None, dev_status=None):
+    """Both caches (sharing one page table) in one launch: the first ``D0``
+    columns of ``rows0`` into ``cache0`` and the first ``D1`` of ``rows1``
+    into ``cache1``, in place."""
+    dev = cache0.device
+    _need(rows0, "rows0", torch.bfloat16, dev, 2)
+    _need(cache0, "cache0", torch.bfloat16, dev, 3)
+    _need(rows1, "rows1", torch.bfloat16, dev, 2)
+    _need(cache1, "cache1", torch.bfloat16, dev, 3)
+    S, PTW = _meta(dev, seq_lens, cu_q_lens, cu_kv_lens, page_indices)
+    T, s0 = rows0.shape
+    T1, s1 = rows1.shape
+    P, ps, c0 = cache0.shape
+    P1, ps1, c1 = cache1.shape
+    if T1 != T or P1 != P or ps1 != ps:
+        raise ValueError("dsa_paged_write_back_pair: both targets need the same tokens, pages and page size")
+    D0 = min(s0, c0) if D0 is None else D0
+    D1 = min(s1, c1) if D1 is None else D1
+    rc = lib().dsa_paged_write_back_pair(_stream(dev), _ptr(rows0), s0, D0, _ptr(cache0), c0, _ptr(rows1), s1, D1,
+                                         _ptr(cache1), c1, _ptr(seq_lens), _ptr(cu_q_lens), _ptr(cu_kv_lens),
+                                         _ptr(page_indices), T, S, P, PTW, ps, _ptr(dev_status))
+    _check("dsa_paged_write_back_pair", rc)
+    return cache0, cache1
 
 
 def dsa_topk_pages_from_tokens(topk, *, ps, max_pages, cap=512, pages=None, counts=None, dev_status=None):

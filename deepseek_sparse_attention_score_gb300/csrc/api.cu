@@ -182,14 +182,42 @@ int dsa_paged_write_back(dsa_stream_t stream, const uint16_t* rows, int src_stri
                          const int32_t* cu_kv_lens, const int32_t* page_indices, int T, int S, int P, int PTW,
                          int ps, int32_t* dev_status) {
   NvtxRange nvtx_range("dsa_paged_write_back");
-  if (T < 0 || S < 0 || P < 0 || PTW < 0 || D < 0) return DSA_ERR_INVALID_ARGUMENT;
-  if (T == 0 || D == 0) return DSA_OK;
-  if (S < 1 || P < 1 || PTW < 1 || ps < 1) return DSA_ERR_INVALID_ARGUMENT;
-  if (!rows || !cache || !seq_lens || !cu_q_lens || !cu_kv_lens || !page_indices) return DSA_ERR_INVALID_ARGUMENT;
+  return dsa_paged_write_back_pair(stream, rows, src_stride, D, cache, cache_stride, nullptr, 0, 0, nullptr, 0,
+                                   seq_lens, cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps, dev_status);
+}
+
+static int write_back_target_check(const uint16_t* rows, int src_stride, int D, uint16_t* cache, int cache_stride) {
+  if (D < 0) return DSA_ERR_INVALID_ARGUMENT;
+  if (D == 0) return DSA_OK;
+  if (!rows || !cache) return DSA_ERR_INVALID_ARGUMENT;
   if (D % 8 || src_stride % 8 || cache_stride % 8 || D > src_stride || D > cache_stride) return DSA_ERR_UNSUPPORTED;
   if (!aligned16(rows) || !aligned16(cache)) return DSA_ERR_ALIGNMENT;
-  return run_paged_write_back(static_cast<cudaStream_t>(stream), rows, src_stride, D, cache, cache_stride, seq_lens,
-                              cu_q_lens, cu_kv_lens, page_indices, T, S, P, PTW, ps, dev_status);
+  return DSA_OK;
+}
+
+int dsa_paged_write_back_pair(dsa_stream_t stream, const uint16_t* rows0, int src_stride0, int D0, uint16_t* cache0,
+                              int cache_stride0, const uint16_t* rows1, int src_stride1, int D1, uint16_t* cache1,
+                              int cache_stride1, const int32_t* seq_lens, const int32_t* cu_q_lens,
+                              const int32_t* cu_kv_lens, const int32_t* page_indices, int T, int S, int P, int PTW,
+                              int ps, int32_t* dev_status) {
+  if (T < 0 || S < 0 || P < 0 || PTW < 0) return DSA_ERR_INVALID_ARGUMENT;
+  int rc = write_back_target_check(rows0, src_stride0, D0, cache0, cache_stride0);
+  if (rc) return rc;
+  if (rows1 || cache1 || D1) {
+    rc = write_back_target_check(rows1, src_stride1, D1, cache1, cache_stride1);
+    if (rc) return rc;
+  }
+  if (T == 0 || D0 == 0) {
+    if (D1 == 0 || T == 0) return DSA_OK;
+    // only the second cache: write it as the first
+    rows0 = rows1, src_stride0 = src_stride1, D0 = D1, cache0 = cache1, cache_stride0 = cache_stride1;
+    rows1 = nullptr, cache1 = nullptr, D1 = 0;
+  }
+  if (S < 1 || P < 1 || PTW < 1 || ps < 1) return DSA_ERR_INVALID_ARGUMENT;
+  if (!seq_lens || !cu_q_lens || !cu_kv_lens || !page_indices) return DSA_ERR_INVALID_ARGUMENT;
+  return run_paged_write_back(static_cast<cudaStream_t>(stream), rows0, src_stride0, D0, cache0, cache_stride0, rows1,
+                              src_stride1, D1, cache1, cache_stride1, seq_lens, cu_q_lens, cu_kv_lens, page_indices,
+                              T, S, P, PTW, ps, dev_status);
 }
 long long dsa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 

@@ -51,10 +51,12 @@ int run_block_union(cudaStream_t stream, const int32_t* topk_units, int T, int K
                     uint32_t* member, int32_t* counts, int32_t* dev_status);
 
 // Paged write-back of new token rows (writeback.cu).
+// one or two caches sharing the page table (rows1 == NULL: one)
 int run_paged_write_back(cudaStream_t stream, const uint16_t* rows, long long src_stride, int D, uint16_t* cache,
-                         long long cache_stride, const int32_t* seq_lens, const int32_t* cu_q_lens,
-                         const int32_t* cu_kv_lens, const int32_t* page_indices, int T, int S, int P, int PTW,
-                         int ps, int32_t* dev_status);
+                         long long cache_stride, const uint16_t* rows1, long long src_stride1, int D1,
+                         uint16_t* cache1, long long cache_stride1, const int32_t* seq_lens,
+                         const int32_t* cu_q_lens, const int32_t* cu_kv_lens, const int32_t* page_indices, int T,
+                         int S, int P, int PTW, int ps, int32_t* dev_status);
 
 // Token top-k -> sorted unique page list per query (pages.cu).
 int topk_pages_max_pages();

@@ -79,10 +79,12 @@ class LayerRunner:
     def write_back(self, layer):
         """The layer's new latent rows, and on a full layer its new indexer
         keys, into their slots of the paged caches."""
-        abi.dsa_paged_write_back(self.new_kv[layer], self.kv[layer], *self.meta, D=576, dev_status=self.status)
-        if self.full_slot[layer] >= 0:
+        if self.full_slot[layer] >= 0:  # both caches share the page table: one launch
             slot = self.full_slot[layer]
-            abi.dsa_paged_write_back(self.new_k[slot], self.kcache[slot], *self.meta, D=128, dev_status=self.status)
+            abi.dsa_paged_write_back_pair(self.new_kv[layer], self.kv[layer], self.new_k[slot], self.kcache[slot],
+                                          *self.meta, D0=576, D1=128, dev_status=self.status)
+        else:
+            abi.dsa_paged_write_back(self.new_kv[layer], self.kv[layer], *self.meta, D=576, dev_status=self.status)
 
     def index(self, slot):
         if self.prefill or self.page_budget is not None:

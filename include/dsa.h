@@ -320,6 +320,23 @@ DSA_API int dsa_paged_write_back(dsa_stream_t stream, const uint16_t* rows, int 
                                  int PTW, int ps, int32_t* dev_status);
 
 /* ------------------------------------------------------------------------
+ * Paged write-back into two caches that share one page table, in one launch
+ * (no counterpart on the pages, which write each cache separately): a
+ * layer's latent rows and, on a full layer, its indexer keys. Each token's
+ * slot is found once; (rows0, src_stride0, D0, cache0, cache_stride0) and
+ * (rows1, ...) follow the rules of dsa_paged_write_back, and both caches
+ * hold P pages of ps rows. rows1 == cache1 == NULL with D1 == 0 writes the
+ * first cache alone (dsa_paged_write_back is that call). Errors as
+ * dsa_paged_write_back, for either target.
+ * ------------------------------------------------------------------------ */
+DSA_API int dsa_paged_write_back_pair(dsa_stream_t stream, const uint16_t* rows0, int src_stride0, int D0,
+                                      uint16_t* cache0, int cache_stride0, const uint16_t* rows1, int src_stride1,
+                                      int D1, uint16_t* cache1, int cache_stride1, const int32_t* seq_lens,
+                                      const int32_t* cu_q_lens, const int32_t* cu_kv_lens,
+                                      const int32_t* page_indices, int T, int S, int P, int PTW, int ps,
+                                      int32_t* dev_status);
+
+/* ------------------------------------------------------------------------
  * Token top-k -> page list, for the page-level decode shape of the pages.
  * dsa_sparse_backend.py, compute_topk_pages (k_pages_max = 512 there): per
  * query row, the ascending unique pages (position / ps) of the selected

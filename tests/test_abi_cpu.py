@@ -167,6 +167,30 @@ def test_paged_write_back_host_checks(dsa, kw, code):
     assert dsa.lib().dsa_paged_write_back(*_write_back_args(**kw)) == code
 
 
+def _write_back_pair_args(**kw):
+    a = dict(stream=None, rows0=_ptr(), src_stride0=576, D0=576, cache0=_ptr(), cache_stride0=576, rows1=_ptr(),
+             src_stride1=128, D1=128, cache1=_ptr(), cache_stride1=128, seq_lens=_ptr(), cu_q_lens=_ptr(),
+             cu_kv_lens=_ptr(), page_indices=_ptr(), T=4, S=4, P=16, PTW=16, ps=64, dev_status=None)
+    a.update(kw)
+    return list(a.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D1=100), UNSUPPORTED),              # each target moves in 16-byte pieces
+    (dict(D0=640, src_stride0=576), UNSUPPORTED),
+    (dict(cache_stride1=132), UNSUPPORTED),
+    (dict(rows1=None), INVALID),              # a second cache without its rows
+    (dict(cache0=None), INVALID),
+    (dict(page_indices=None), INVALID),
+    (dict(cache1=_ptr(4104)), ALIGNMENT),
+    (dict(T=-1), INVALID),
+    (dict(T=0), OK),
+    (dict(D0=0, D1=0), OK),
+])
+def test_paged_write_back_pair_host_checks(dsa, kw, code):
+    assert dsa.lib().dsa_paged_write_back_pair(*_write_back_pair_args(**kw)) == code
+
+
 def _pages_args(**kw):
     a = dict(stream=None, topk=_ptr(), T=4, K=64, ps=64, max_pages=1024, cap=512, pages=_ptr(), counts=None,
              dev_status=None)

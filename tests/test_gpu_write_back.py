@@ -56,6 +56,29 @@ def test_write_back_matches_oracle(dsa, ps, width, D):
     assert np.array_equal(got, ref)
 
 
+@pytest.mark.parametrize("ps", [32, 64, 128])
+def test_write_back_pair_matches_oracle(dsa, ps):
+    """Both caches of a full layer (latent rows, 576 of 640 columns; indexer
+    keys, 128) written by one launch: each equals the oracle's single-cache
+    write-back, bit for bit."""
+    dev = torch.device("cuda")
+    rng, kv, cu_q, cu_kv, pi, P = _batch(11 + ps, ps, [1, 37, 0, 300, 1], [5000, 700, 64, 300, 1])
+    T = int(cu_q[-1])
+    c0, c1 = _bits(rng, (P, ps, 640)), _bits(rng, (P, ps, 128))
+    r0, r1 = _bits(rng, (T, 576)), _bits(rng, (T, 128))
+    ref0 = O.paged_write_back(c0, r0, kv, cu_q, cu_kv, pi)  # the first 576 columns
+    ref1 = O.paged_write_back(c1, r1, kv, cu_q, cu_kv, pi)
+    to = lambda a: torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    g0, g1, gr0, gr1 = to(c0), to(c1), to(r0), to(r1)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    meta = [torch.from_numpy(a).to(dev) for a in (kv, cu_q, cu_kv, pi)]
+    dsa.dsa_paged_write_back_pair(gr0, g0, gr1, g1, *meta, D0=576, D1=128, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert np.array_equal(g0.view(torch.int16).cpu().numpy().view(np.uint16), ref0)
+    assert np.array_equal(g1.view(torch.int16).cpu().numpy().view(np.uint16), ref1)
+
+
 def test_write_back_reports_bad_page_table(dsa):
     dev = torch.device("cuda")
     rng, kv, cu_q, cu_kv, pi, P = _batch(3, 64, [2, 3], [130, 70])
