@@ -552,7 +552,9 @@ __global__ void __launch_bounds__((6 + kCopyW) * 32, 1)
         for (int l = 0; l < kDk * 2 / 128; ++l) prefetch_l2_line(rp + l * 128);
       }
       if (!more && (j & 1)) {
-        if (!publish(-1, 0u, -1, false)) break;
+        // its first row -32: a page-run box of rows -32..-1 lies wholly
+        // outside the tensor and is zero-filled (no stray cache row is read)
+        if (!publish(-1, 0u, -kSubKeys, false)) break;
       }
       if (!publish(row, mask, base, !more)) break;
       if (!more) break;

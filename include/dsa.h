@@ -173,6 +173,12 @@ DSA_API int dsa_build_block_union(dsa_stream_t stream, const int32_t* topk_units
  *          (split-key partials; 0 bytes needed when T*H is large)
  * Supported: Dk == 576, Dv == 512, row_stride in {576, 640}, ps in
  * {32, 64, 128}, H >= 1 (heads are processed 128 at a time).
+ * Cache contents: with page units (and in the query-block and dense forms)
+ * whole runs of 32 rows of each selected page are read and the rows past
+ * the visible length are masked with a probability of exactly 0, so those
+ * rows (the unwritten tail of a request's last page) must hold finite values
+ * (0 x NaN is NaN), as in the pages' kernels; token units read only the
+ * selected rows.
  * Reproducibility: every output is the same on every run: when a row's
  * keys are split across CTAs (few queries, long selections) the merging CTA
  * adds the splits in a fixed order, whichever CTA of the row finishes last.

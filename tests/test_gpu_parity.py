@@ -241,3 +241,32 @@ def test_tiny_decode_end_to_end(dsa):
     ref_o, _ = O.sparse_mla(f32(wl.q[0]), f32(wl.kv[0]), **meta_np(rg), sel=ref, unit=1, sm_scale=wl.sm_scale,
                             Dv=512)
     check_attention(o, ref_o)
+
+
+@pytest.mark.parametrize("ps", [32, 64])
+def test_page_units_odd_step_count_reads_no_stray_rows(dsa, ps):
+    """A selection with an odd number of 32-key steps is completed by an empty
+    step; its boxes must be zero-filled, not read from the start of the cache
+    (here physical page 0 holds NaN and is selected by nobody)."""
+    dev = torch.device("cuda")
+    wl = DI.random_small(431 + ps, [1, 1], [700, 900], H=16, page_size=ps)
+    rg = wl.rg
+    kv = wl.kv[0].clone()
+    kv.view(torch.int16)[0] = 0x7FC0  # bf16 NaN in every row of physical page 0
+    owner = np.nonzero(rg.page_indices == 0)[0]
+    pages = [np.arange(-(-int(n) // ps)) for n in rg.seq_lens]
+    sel = np.full((rg.T, 3), -1, np.int32)
+    for t in range(rg.T):
+        base = rg.cu_kv_lens[t] // ps
+        ok = [p for p in pages[t] if base + p not in owner]  # pages that are not physical page 0
+        sel[t] = ok[:3]
+    meta = meta_to(rg, dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    o = dsa.dsa_sparse_mla_decode(wl.q[0].to(dev), kv.to(dev), *meta, torch.from_numpy(sel).to(dev), unit=ps,
+                                  sm_scale=wl.sm_scale, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.isfinite(o.float()).all(), "a stray row of page 0 reached the output"
+    ref_o, _ = O.sparse_mla(f32(wl.q[0]), f32(wl.kv[0]), **meta_np(rg), sel=sel, unit=ps, sm_scale=wl.sm_scale,
+                            Dv=512)
+    check_attention(o, ref_o, "odd page steps")
