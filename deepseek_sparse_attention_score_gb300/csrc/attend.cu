@@ -793,10 +793,6 @@ __global__ void __launch_bounds__((6 + kCopyW) * 32, 1)
         for (int j = 0; j < 32; ++j) oa[j] = ob[j] = 0u;
       }
     };
-    auto store_bf16_4 = [&](uint16_t* dst, float4 a) {
-      __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
-      *reinterpret_cast<uint2*>(dst) = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
-    };
     if (prm.nsplit == 1) {
       // one split: the warp stages its 32 head rows as bf16 in the idle key
       // stage (four 128-byte-swizzled boxes of 64 columns) and one lane
@@ -835,14 +831,11 @@ __global__ void __launch_bounds__((6 + kCopyW) * 32, 1)
       __syncwarp();
       if (hv && half == 0 && prm.lse) prm.lse[(size_t)t * prm.H + h] = lse_v;
     } else {
-      // split keys: write this split's normalised partial; the last CTA of the
-      // (token, value half) group merges all splits and writes the output.
-      // O leaves TMEM through shared memory: each thread puts its head row
-      // (scaled by 1/l) into its warp's slice of the stage, then the warp
-      // writes one row at a time, 32 lanes over consecutive 16-byte pieces,
-      // so that every store and every load of the merge covers whole cache
-      // lines. The stage reuses the Q and key buffers, idle once the last PV
-      // has completed.
+      // split keys: each CTA stages its normalised partial (rows scaled by
+      // 1/l) in shared memory; below, every warp of the CTA writes it out and,
+      // in the last CTA of the (token, value half) group, merges all splits.
+      // The stage reuses the Q and key buffers, idle once the last PV has
+      // completed; its rows are padded to 1040 bytes against bank conflicts.
       float* stg = reinterpret_cast<float*>(smem + OFF_STAGE) + (warp & 3) * 32 * kStageLd;
 #pragma unroll 1
       for (int c0 = 0; c0 < kDvHalf; c0 += 64) {
@@ -857,116 +850,10 @@ __global__ void __launch_bounds__((6 + kCopyW) * 32, 1)
                                     __uint_as_float(ob[4 * v + 2]) * inv_l, __uint_as_float(ob[4 * v + 3]) * inv_l);
         }
       }
-      __syncwarp();
-      // rows of this warp that exist (h < H); uniform over the warp
-      const int hw = h0 + (warp & 3) * 32;
-      const int nrows = max(0, min(32, prm.H - hw));
-      const size_t orow0 = ((size_t)t * prm.H + hw) * kDv + half * kDvHalf;  // element offset of row hw
-      float* op = prm.o_part + ((size_t)split * prm.T * prm.H) * kDv + orow0;
-#pragma unroll 2
-      for (int i = 0; i < nrows; ++i) {
-        const float* sr = stg + i * kStageLd;
-        float4* dst = reinterpret_cast<float4*>(op + (size_t)i * kDv);
-        dst[lane] = *reinterpret_cast<const float4*>(sr + 4 * lane);
-        dst[32 + lane] = *reinterpret_cast<const float4*>(sr + 128 + 4 * lane);
-      }
       // lse of this split as seen by this CTA (both value halves compute the
       // same logits, so each group merges with its own copies)
-      float* lsep = prm.lse_part + (size_t)gridDim.x * 128;
-      lsep[(((size_t)split * prm.T + t) * gridDim.x + blockIdx.x) * 128 + r] = lse_v;
-      __threadfence();
-      named_bar_sync(2, 128);
-      volatile int* s_last = abort_flag + 1;
-      if (r == 0) {
-        int* ctr = prm.counters + (size_t)t * gridDim.x + blockIdx.x;
-        const int old = atomicAdd(ctr, 1);
-        const int last = old == prm.nsplit - 1;
-        if (last) *ctr = 0;  // ready for the next call
-        *s_last = last;
-      }
-      named_bar_sync(2, 128);
-      if (*s_last) {  // uniform over the CTA
-        __threadfence();
-        // per head row (this thread's): the weight of each split's partial,
-        // kept in shared memory for the warp-wide merge below
-        float* wts = reinterpret_cast<float*>(smem + OFF_WTS);
-        auto lse_of = [&](int z) {
-          return __ldcg(lsep + (((size_t)z * prm.T + t) * gridDim.x + blockIdx.x) * 128 + r);
-        };
-        float mx = -INFINITY;
-#pragma unroll 1
-        for (int z = 0; z < prm.nsplit; ++z) mx = fmaxf(mx, lse_of(z));
-        float tot = 0.f;
-#pragma unroll 1
-        for (int z = 0; z < prm.nsplit; ++z) {
-          const float lz = lse_of(z);
-          const float w = (mx == -INFINITY || lz == -INFINITY) ? 0.f : exp2f((lz - mx) * 1.4426950408889634f);
-          wts[z * 128 + r] = w;
-          tot += w;
-        }
-        const float inv = tot > 0.f ? 1.f / tot : 0.f;
-#pragma unroll 1
-        for (int z = 0; z < prm.nsplit; ++z) wts[z * 128 + r] *= inv;
-        if (hv && half == 0 && prm.lse) prm.lse[(size_t)t * prm.H + h] = tot > 0.f ? mx + logf(tot) : -INFINITY;
-        __syncwarp();
-        // the warp merges its 32 rows, four at a time; this CTA's own split
-        // is read from the stage, the others from the partials. The splits
-        // are added in the fixed order 0, 1, ..., so a decode output does not
-        // depend on which CTA of its row merges (measured: no cost in the
-        // page-run instantiation since its copier and ring changed; it had
-        // cost 2-3% through code layout before)
-        const int rw = (warp & 3) * 32;  // first row of this warp
-        const float* parts = prm.o_part + orow0;
-        const size_t zstride = (size_t)prm.T * prm.H * kDv;
-#pragma unroll 1
-        for (int i0 = 0; i0 < nrows; i0 += 4) {
-          float4 acc[4][2];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            acc[u][0] = make_float4(0.f, 0.f, 0.f, 0.f);
-            acc[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-#pragma unroll 1
-          for (int z = 0; z < prm.nsplit; ++z) {
-            float4 va[4][2];
-            if (z == split) {
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const float* sr = stg + (i0 + u) * kStageLd;
-                va[u][0] = *reinterpret_cast<const float4*>(sr + 4 * lane);
-                va[u][1] = *reinterpret_cast<const float4*>(sr + 128 + 4 * lane);
-              }
-            } else {
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const bool live = i0 + u < nrows;
-                const float4* src = reinterpret_cast<const float4*>(parts + z * zstride + (size_t)(i0 + u) * kDv);
-                va[u][0] = live ? __ldcg(src + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
-                va[u][1] = live ? __ldcg(src + 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
-              }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float w = wts[z * 128 + rw + i0 + u];
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                acc[u][e].x = fmaf(w, va[u][e].x, acc[u][e].x);
-                acc[u][e].y = fmaf(w, va[u][e].y, acc[u][e].y);
-                acc[u][e].z = fmaf(w, va[u][e].z, acc[u][e].z);
-                acc[u][e].w = fmaf(w, va[u][e].w, acc[u][e].w);
-              }
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            if (i0 + u < nrows) {
-              uint16_t* dst = prm.o + orow0 + (size_t)(i0 + u) * kDv;
-              store_bf16_4(dst + 4 * lane, acc[u][0]);
-              store_bf16_4(dst + 128 + 4 * lane, acc[u][1]);
-            }
-          }
-        }
-      }
+      prm.lse_part[(size_t)gridDim.x * 128 + (((size_t)split * prm.T + t) * gridDim.x + blockIdx.x) * 128 + r] =
+          lse_v;
     }
   }
   tc_fence_before();
@@ -978,6 +865,125 @@ __global__ void __launch_bounds__((6 + kCopyW) * 32, 1)
     }
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  if (prm.nsplit > 1) {
+    // Split keys, with every warp of the CTA (the staged partial is complete
+    // and every role has finished at the barrier above). A warp moves one
+    // 1 KB head row at a time, 32 lanes over consecutive 16-byte pieces, so
+    // that every store and every load covers whole cache lines; the merge
+    // runs its loads on all warps because each round of them waits on L2
+    // (on the four softmax warps alone the merging CTA took about twice as
+    // long as the others).
+    const int nw = (int)(blockDim.x >> 5);
+    const float* stg = reinterpret_cast<const float*>(smem + OFF_STAGE);
+    const int nrows = max(0, min(128, prm.H - h0));  // head rows that exist
+    const size_t orow0 = ((size_t)t * prm.H + h0) * kDv + half * kDvHalf;  // element offset of row h0
+    const size_t zstride = (size_t)prm.T * prm.H * kDv;
+    float* op = prm.o_part + (size_t)split * zstride + orow0;
+#pragma unroll 2
+    for (int i = warp; i < nrows; i += nw) {
+      const float* sr = stg + i * kStageLd;
+      float4* dst = reinterpret_cast<float4*>(op + (size_t)i * kDv);
+      dst[lane] = *reinterpret_cast<const float4*>(sr + 4 * lane);
+      dst[32 + lane] = *reinterpret_cast<const float4*>(sr + 128 + 4 * lane);
+    }
+    __threadfence();
+    __syncthreads();
+    volatile int* s_last = abort_flag + 1;
+    if (tid == 0) {
+      int* ctr = prm.counters + (size_t)t * gridDim.x + blockIdx.x;
+      const int old = atomicAdd(ctr, 1);
+      const int last = old == prm.nsplit - 1;
+      if (last) *ctr = 0;  // ready for the next call
+      *s_last = last;
+    }
+    __syncthreads();
+    if (*s_last) {  // uniform over the CTA
+      __threadfence();
+      // per head row: the weight of each split's partial, in shared memory
+      float* wts = reinterpret_cast<float*>(smem + OFF_WTS);
+      if (tid < 128) {
+        const float* lsep = prm.lse_part + (size_t)gridDim.x * 128;
+        auto lse_of = [&](int z) {
+          return __ldcg(lsep + (((size_t)z * prm.T + t) * gridDim.x + blockIdx.x) * 128 + tid);
+        };
+        float mx = -INFINITY;
+#pragma unroll 1
+        for (int z = 0; z < prm.nsplit; ++z) mx = fmaxf(mx, lse_of(z));
+        float tot = 0.f;
+#pragma unroll 1
+        for (int z = 0; z < prm.nsplit; ++z) {
+          const float lz = lse_of(z);
+          const float w = (mx == -INFINITY || lz == -INFINITY) ? 0.f : exp2f((lz - mx) * 1.4426950408889634f);
+          wts[z * 128 + tid] = w;
+          tot += w;
+        }
+        const float inv = tot > 0.f ? 1.f / tot : 0.f;
+#pragma unroll 1
+        for (int z = 0; z < prm.nsplit; ++z) wts[z * 128 + tid] *= inv;
+        if (tid < nrows && half == 0 && prm.lse)
+          prm.lse[(size_t)t * prm.H + h0 + tid] = tot > 0.f ? mx + logf(tot) : -INFINITY;
+      }
+      __syncthreads();
+      // every warp merges groups of four rows; this CTA's own split is read
+      // from the stage, the others from the partials. The splits are added
+      // in the fixed order 0, 1, ..., so an output does not depend on which
+      // CTA of its row merges.
+      auto store_bf16_4 = [&](uint16_t* dst, float4 a) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
+        *reinterpret_cast<uint2*>(dst) =
+            make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+      };
+      const float* parts = prm.o_part + orow0;
+#pragma unroll 1
+      for (int i0 = 4 * warp; i0 < nrows; i0 += 4 * nw) {
+        float4 acc[4][2];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          acc[u][0] = make_float4(0.f, 0.f, 0.f, 0.f);
+          acc[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll 1
+        for (int z = 0; z < prm.nsplit; ++z) {
+          float4 va[4][2];
+          if (z == split) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float* sr = stg + (i0 + u) * kStageLd;
+              va[u][0] = *reinterpret_cast<const float4*>(sr + 4 * lane);
+              va[u][1] = *reinterpret_cast<const float4*>(sr + 128 + 4 * lane);
+            }
+          } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const bool live = i0 + u < nrows;
+              const float4* src = reinterpret_cast<const float4*>(parts + z * zstride + (size_t)(i0 + u) * kDv);
+              va[u][0] = live ? __ldcg(src + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+              va[u][1] = live ? __ldcg(src + 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float w = wts[z * 128 + i0 + u];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              acc[u][e].x = fmaf(w, va[u][e].x, acc[u][e].x);
+              acc[u][e].y = fmaf(w, va[u][e].y, acc[u][e].y);
+              acc[u][e].z = fmaf(w, va[u][e].z, acc[u][e].z);
+              acc[u][e].w = fmaf(w, va[u][e].w, acc[u][e].w);
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (i0 + u < nrows) {
+            uint16_t* dst = prm.o + orow0 + (size_t)(i0 + u) * kDv;
+            store_bf16_4(dst + 4 * lane, acc[u][0]);
+            store_bf16_4(dst + 128 + 4 * lane, acc[u][1]);
+          }
+        }
+      }
+    }
   }
 }
 
